@@ -1,0 +1,437 @@
+"""Benchmark of the calibration-Hessian hot path on one GB300.
+
+One step = reset the accumulator, add every batch of the workload through
+the C ABI (the queue fuses them into split-K SYRK passes), and materialize
+the damped fp32 Hessian.  Inputs are synthetic, seeded and resident in HBM
+before the timed region; they are larger than L2, so no flush is needed.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Hessian-accum TFLOP/s & tokens/s at d=4096 (1 GB300); % of BF16/HBM roofline"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algo_flops(n_tokens, d):
+    return float(n_tokens) * d * (d + 1)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-i", str(self._index())],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    @staticmethod
+    def _index():
+        import torch
+        return torch.cuda.current_device()
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+            sm = [float(r[1]) for r in rows]
+            mx = [float(r[2]) for r in rows]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i]})
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
+                    "samples": len(rows)}
+        except Exception as e:  # pragma: no cover
+            return {"error": str(e)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------- ours
+
+
+def run_ours(args):
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+
+    ws, rank = dist_init()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    hbm, bf16_burst, bf16_sust, peak_src = peaks()
+    wl = WORKLOADS[args.workload]
+    d = wl.d
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    n_tok = wl.n_tokens
+    flops = algo_flops(n_tok, d)
+    h = Hessian(d)
+    out = torch.empty((d, d), dtype=torch.float32, device="cuda")
+
+    def step():
+        h.reset()
+        for X in xs:
+            h.add_batch(X)
+        h.materialize(wl.damp_percent, out=out, want_damp=False)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = _count_flushes(h, xs) + 2  # SYRK passes + diag + materialize
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, ws)
+    value = ws * flops / (ms * 1e-3) / 1e12
+
+    # dominant kernel: the fused SYRK passes, timed with events around every
+    # call that triggered a flush (the GPU stays busy between them)
+    kern = _time_syrk(h, xs, reps=3)
+    syrk_tflops = flops / kern["seconds"] / 1e12
+    e2e = _e2e(h, wl, xs, d, args)
+
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+        "tokens_per_s": round(ws * n_tok / (ms * 1e-3), 1),
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch.randn, per-channel std log-uniform [0.1, 10], rounded to bf16)",
+        "config": {"workload": wl.name, "d": d, "batches": len(xs), "tokens": n_tok,
+                   "token_counts": "uniform integers [1, 2000], numpy default_rng(3)",
+                   "damp_percent": wl.damp_percent, "flops_counted": "N*d*(d+1) (upper triangle)",
+                   "l2": "inputs (%.2f GB) larger than L2; no flush" % (n_tok * d * 2 / 1e9),
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(syrk_tflops, 2), "peak": bf16_sust,
+                     "unit": "TFLOP/s", "frac": round(syrk_tflops / bf16_sust, 4), "traffic": None,
+                     "kernel": "syrk_bf16_kernel",
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16, dense)",
+                     "launches_timed": kern["launches"]},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_extra:
+        res["extra"] = _extra(args, hbm, bf16_burst, bf16_sust)
+    if rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    h.close()
+    if rank == 0:
+        print(json.dumps(res))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _count_flushes(h, xs):
+    h.reset()
+    n = 0
+    for X in xs:
+        before = len(h._queued)
+        h.add_batch(X)
+        if len(h._queued) < before + 1:
+            n += 1
+    if h._queued:
+        n += 1
+    h.flush()
+    return n
+
+
+def _time_syrk(h, xs, reps=3):
+    import torch
+    pairs = []
+    for _ in range(reps):
+        h.reset()
+        for X in xs:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            h.add_batch(X)
+            if not h._queued:
+                b.record()
+                pairs.append((a, b))
+        if h._queued:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            h.flush()
+            b.record()
+            pairs.append((a, b))
+    torch.cuda.synchronize()
+    total = sum(a.elapsed_time(b) for a, b in pairs) * 1e-3 / reps
+    return {"seconds": total, "launches": len(pairs) // reps}
+
+
+def _e2e(h, wl, xs, d, args):
+    """Same metric through the public API with host buffers: pinned-host ->
+    device copies of every batch and the device -> host read of H inside the
+    timed region."""
+    import torch
+    host_x = [X.cpu().pin_memory() for X in xs]
+    dev_x = [torch.empty_like(X) for X in xs]
+    out = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    host_h = torch.empty((d, d), dtype=torch.float32).pin_memory()
+    flops = algo_flops(wl.n_tokens, d)
+
+    def step():
+        h.reset()
+        for hx, dx in zip(host_x, dev_x):
+            dx.copy_(hx, non_blocking=True)
+            h.add_batch(dx)
+        h.materialize(wl.damp_percent, out=out, want_damp=False)
+        host_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(flops / dt / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in xs)),
+            "d2h_bytes_per_step": int(d * d * 4), "ms_per_step": round(dt * 1e3, 3)}
+
+
+def _extra(args, hbm, bf16_burst, bf16_sust):
+    """Secondary workloads: the compute-bound large-batch Gram and the
+    HBM-bound local 16x16 blocks, each with its own roofline."""
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    out = {}
+    # large batches: 16 updates of 32768 tokens at d = 4096
+    wl = WORKLOADS["d4096_16x32768"]
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    h = Hessian(wl.d)
+    Hm = torch.empty((wl.d, wl.d), dtype=torch.float32, device="cuda")
+
+    def run():
+        h.reset()
+        for X in xs:
+            h.add_batch(X)
+        h.flush()
+    run()
+    torch.cuda.synchronize()
+    kern = _time_syrk(h, xs, reps=3)
+    fl = algo_flops(wl.n_tokens, wl.d)
+    t = kern["seconds"]
+    out["large_batch_gram"] = {
+        "workload": wl.name, "tflops": round(fl / t / 1e12, 2), "ms": round(t * 1e3, 3),
+        "tokens_per_s": round(wl.n_tokens / t, 1),
+        "roofline": {"bound": "tensor", "peak": bf16_burst, "unit": "TFLOP/s",
+                     "frac": round(fl / t / 1e12 / bf16_burst, 4), "peak_source": "bf16_tflops (burst)"}}
+    h.close()
+    del xs
+    # local_hessian: 8 updates of 32768 tokens at d = 4096
+    wl = WORKLOADS["local_d4096_8x32768"]
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    lh = LocalHessian(wl.d)
+    for X in xs:
+        lh.add_batch(X)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(3):
+        for X in xs:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            lh.add_batch(X)
+            b.record()
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    per = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e-3
+    nbytes = xs[0].numel() * 2
+    out["local_hessian"] = {
+        "workload": wl.name, "us_per_update": round(per * 1e6, 2),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / per / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(nbytes / per / 1e9 / hbm, 4),
+                     "bytes_per_update": nbytes, "kernel": "local_gram_kernel"}}
+    lh.close()
+    return out
+
+
+# --------------------------------------------------------------- reference
+
+
+def cpu_baseline(wl, budget_s=15.0):
+    """The float64 oracle on the host cores, over as many leading batches of
+    the workload as fit the time budget."""
+    import torch
+
+    from oracle import GramOracle
+    from gptq_qqq_calibration_gb300.synthetic import make_batch
+    o = GramOracle(wl.d)
+    t_used, n_used, nb = 0.0, 0, 0
+    for b, n in enumerate(wl.token_counts):
+        X = make_batch(int(n), wl.d, wl.batch_seed(b), profile=wl.profile, profile_seed=wl.seed,
+                       dtype=torch.bfloat16).to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        o.add_batch(X)
+        t_used += time.perf_counter() - t0
+        n_used += int(n)
+        nb += 1
+        if t_used >= budget_s:
+            break
+    t0 = time.perf_counter()
+    o.materialize(wl.damp_percent)
+    t_used += time.perf_counter() - t0
+    return {"value": round(algo_flops(n_used, wl.d) / t_used / 1e12, 5), "unit": "TFLOP/s",
+            "tokens_per_s": round(n_used / t_used, 1), "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"first {nb} of {len(wl.token_counts)} batches ({n_used} tokens) of {wl.name}, "
+                      f"float64 NumPy X^T X + materialize, {t_used:.1f} s"}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max(i.get("num_threads", 1) for i in threadpool_info())
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    from oracle import GramOracle
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS, make_batch
+    wl = WORKLOADS[args.workload]
+    per_step = max(1, args.ref_batches)
+    xs = [make_batch(int(n), wl.d, wl.batch_seed(b), profile=wl.profile, profile_seed=wl.seed,
+                     dtype=torch.bfloat16).to(torch.float64).numpy()
+          for b, n in enumerate(wl.token_counts[:per_step])]
+    n_tok = sum(x.shape[0] for x in xs)
+
+    def step():
+        o = GramOracle(wl.d)
+        for X in xs:
+            o.add_batch(X)
+        o.materialize(wl.damp_percent)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = algo_flops(n_tok, wl.d) / dt / 1e12
+    cores = _blas_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "d": wl.d, "sample_batches": per_step,
+                                        "sample_tokens": n_tok},
+        "cpu_baseline": {"value": round(v, 5), "unit": "TFLOP/s", "kind": "oracle", "cores": cores,
+                         "sample": f"first {per_step} batches ({n_tok} tokens) of {wl.name} per step"},
+        "e2e": {"value": round(v, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="d4096_ragged360_loguniform")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-batches", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        from gptq_qqq_calibration_gb300 import build as b
+        b.build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,593 @@
+// Host side of the C ABI declared in include/hess.h: handles, argument
+// validation, the ragged-batch queue, tensor-map encoding and launches.
+//
+// Queue: hess_add_batch only records (pointer, tokens, stream).  A flush
+// turns every queued batch of one dtype into one tensor map, concatenates
+// their tokens into one stream of 64-token k-blocks and runs a single
+// split-K SYRK pass over it, so the accumulator is read and written once per
+// flush instead of once per batch (GPTQModel PR #2981, Changes: no transient
+// d x d product per batch; the accumulator is allocated once).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "hess.h"
+#include "kernels.cuh"
+
+#define HESS_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_last_error;
+
+hess_status fail(hess_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+#define CUDA_TRY(call)                                                                         \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail(HESS_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
+    } while (0)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major [rows, cols] tensor map with a 128-byte-swizzled box of
+// box_cols x box_rows elements; reads past the edges return zeros.
+hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, size_t elem,
+                      int64_t cols, int64_t rows, uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(HESS_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(HESS_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld]",
+                    static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols));
+    return HESS_OK;
+}
+
+// Per-device one-time kernel set-up (dynamic shared-memory limits).
+hess_status prepare_device(int dev) {
+    static std::mutex mu;
+    static bool done[128] = {};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 128) return fail(HESS_ERR_UNSUPPORTED, "device index %d", dev);
+    if (done[dev]) return HESS_OK;
+    CUDA_TRY(hk::syrk_bf16_prepare());
+    CUDA_TRY(hk::syrk_f32_prepare());
+    CUDA_TRY(hk::local_prepare());
+    done[dev] = true;
+    return HESS_OK;
+}
+
+bool injected_alloc_failure() {
+    const char* f = std::getenv("HESS_FAULT");
+    return f && std::strcmp(f, "alloc") == 0;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+struct hess_ctx {
+    std::mutex mu;
+    int device = 0;
+    int64_t d = 0;
+    int T = 0;
+    int n_tiles = 0;
+    int sm_count = 0;
+    double* acc = nullptr;
+    uint32_t* status = nullptr;
+    double* damp64 = nullptr;
+    float* damp32 = nullptr;
+    cudaEvent_t ev = nullptr;
+    int64_t N = 0;
+    struct Pending {
+        const void* ptr;
+        int64_t n;
+        cudaStream_t stream;
+    };
+    std::vector<Pending> pending;
+    int32_t pending_dtype = -1;
+    int64_t pending_tokens = 0;
+    // options
+    int64_t flush_tokens = 65536;
+    int max_pending = hk::kMaxBatches;
+    int chunk_tokens = 1024;
+    unsigned long long timeout_ns = 2000000000ull;
+    int split_k = 0;
+    int grid = 0;
+    hk::SyrkParams* params = nullptr;  // host staging of the launch parameters
+};
+
+struct local_hess_ctx {
+    std::mutex mu;
+    int device = 0;
+    int64_t d = 0;
+    int block = 16;
+    int n_blocks = 0;
+    int sm_count = 0;
+    double* acc = nullptr;
+    uint32_t* status = nullptr;
+    int64_t N = 0;
+    unsigned long long timeout_ns = 2000000000ull;
+};
+
+namespace {
+
+hess_status check_device(int dev) {
+    int cur = -1;
+    CUDA_TRY(cudaGetDevice(&cur));
+    if (cur != dev)
+        return fail(HESS_ERR_INVALID, "handle belongs to device %d but device %d is current", dev, cur);
+    return HESS_OK;
+}
+
+// Split-K factor: the fewest token slabs that keep >= 90 % of the grid busy
+// over all waves of (tile, slab) units.
+int choose_slabs(int n_tiles, int total_kb, int grid) {
+    const int smax = std::max(1, std::min(64, total_kb / 2));
+    int best = 1;
+    double best_eff = 0.0;
+    for (int S = 1; S <= smax; ++S) {
+        const long long units = static_cast<long long>(n_tiles) * S;
+        const long long waves = (units + grid - 1) / grid;
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * grid);
+        if (eff >= 0.9) return S;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    return best;
+}
+
+hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
+    if (h->pending.empty()) return HESS_OK;
+    // Order the flush after the work that produced every queued batch.
+    for (size_t i = 0; i < h->pending.size(); ++i) {
+        cudaStream_t s = h->pending[i].stream;
+        if (s == stream) continue;
+        bool seen = false;
+        for (size_t k = 0; k < i; ++k) seen |= h->pending[k].stream == s;
+        if (seen) continue;
+        CUDA_TRY(cudaEventRecord(h->ev, s));
+        CUDA_TRY(cudaStreamWaitEvent(stream, h->ev, 0));
+    }
+    hk::SyrkParams& p = *h->params;
+    const bool f32 = h->pending_dtype == HESS_F32;
+    const int nb = static_cast<int>(h->pending.size());
+    p.kb_start[0] = 0;
+    for (int b = 0; b < nb; ++b) {
+        const auto& q = h->pending[b];
+        hess_status st =
+            f32 ? encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, h->d, q.n, 32,
+                            hk::kKBlock)
+                : encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->d, q.n, 64,
+                            hk::kKBlock);
+        if (st != HESS_OK) return st;
+        p.kb_start[b + 1] = p.kb_start[b] + static_cast<int32_t>(ceil_div(q.n, hk::kKBlock));
+    }
+    p.n_batches = nb;
+    p.total_kb = p.kb_start[nb];
+    p.n_tiles = h->n_tiles;
+    p.tiles_per_dim = h->T;
+    p.chunk_kb = std::max(1, h->chunk_tokens / hk::kKBlock);
+    p.d = static_cast<int32_t>(h->d);
+    p.acc = h->acc;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
+    p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
+                               : choose_slabs(h->n_tiles, p.total_kb, grid_max);
+    p.n_units = p.n_tiles * p.n_slabs;
+    const int grid = std::min(grid_max, p.n_units);
+    cudaError_t e = f32 ? hk::launch_syrk_f32(p, grid, stream) : hk::launch_syrk_bf16(p, grid, stream);
+    h->pending.clear();
+    h->pending_tokens = 0;
+    h->pending_dtype = -1;
+    if (e != cudaSuccess) return fail(HESS_ERR_CUDA, "SYRK launch failed: %s", cudaGetErrorString(e));
+    if (std::getenv("HESS_TRACE"))
+        std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d grid=%d %s\n",
+                     static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, grid,
+                     f32 ? "f32" : "bf16");
+    return HESS_OK;
+}
+
+hess_status read_status(uint32_t* dev_status, cudaStream_t stream) {
+    uint32_t st = 0;
+    CUDA_TRY(cudaMemcpyAsync(&st, dev_status, sizeof(st), cudaMemcpyDeviceToHost, stream));
+    CUDA_TRY(cudaStreamSynchronize(stream));
+    if (st != 0) return fail(HESS_ERR_TIMEOUT, "a device-side wait ran out (status 0x%x)", st);
+    return HESS_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ full H
+
+HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d <= 0) return fail(HESS_ERR_INVALID, "d must be positive (got %lld)", (long long)d);
+    if (d > 32768) return fail(HESS_ERR_UNSUPPORTED, "d = %lld exceeds 32768", (long long)d);
+    if (d % 8 != 0) return fail(HESS_ERR_UNSUPPORTED, "d = %lld is not a multiple of 8", (long long)d);
+    if (injected_alloc_failure()) return fail(HESS_ERR_OOM, "injected allocation failure (HESS_FAULT=alloc)");
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    hess_status st = prepare_device(dev);
+    if (st != HESS_OK) return st;
+    hess_ctx* h = new (std::nothrow) hess_ctx();
+    if (!h) return fail(HESS_ERR_OOM, "host allocation failed");
+    h->params = new (std::nothrow) hk::SyrkParams();
+    if (!h->params) {
+        delete h;
+        return fail(HESS_ERR_OOM, "host allocation failed");
+    }
+    h->device = dev;
+    h->d = d;
+    h->T = static_cast<int>(ceil_div(d, hk::kTile));
+    h->n_tiles = h->T * (h->T + 1) / 2;
+    cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    const size_t acc_bytes = static_cast<size_t>(h->n_tiles) * hk::kTileElems * sizeof(double);
+    if (e == cudaSuccess) e = cudaMalloc(&h->acc, acc_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&h->status, 64);
+    if (e == cudaSuccess) e = cudaMalloc(&h->damp64, sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc(&h->damp32, sizeof(float));
+    if (e == cudaSuccess) e = cudaMemset(h->acc, 0, acc_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
+        cudaFree(h->acc);
+        cudaFree(h->status);
+        cudaFree(h->damp64);
+        cudaFree(h->damp32);
+        if (h->ev) cudaEventDestroy(h->ev);
+        delete h->params;
+        delete h;
+        return fail(s, "hess_create: %s", cudaGetErrorString(e));
+    }
+    *out = h;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens, int32_t dtype,
+                                       hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (n_tokens < 0) return fail(HESS_ERR_INVALID, "n_tokens < 0");
+    if (dtype != HESS_BF16 && dtype != HESS_F32) return fail(HESS_ERR_INVALID, "unknown dtype %d", dtype);
+    if (n_tokens == 0) return HESS_OK;  // empty batch: no-op, N unchanged
+    if (!X) return fail(HESS_ERR_INVALID, "X is NULL with n_tokens > 0");
+    if (reinterpret_cast<uintptr_t>(X) % 16 != 0) return fail(HESS_ERR_INVALID, "X is not 16-byte aligned");
+    if (n_tokens > (int64_t(1) << 31) - hk::kKBlock)
+        return fail(HESS_ERR_UNSUPPORTED, "n_tokens exceeds 2^31 - 64 in one batch");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!h->pending.empty()) {
+        const int64_t kb_now = ceil_div(n_tokens, hk::kKBlock);
+        int64_t kb_pending = 0;
+        for (const auto& q : h->pending) kb_pending += ceil_div(q.n, hk::kKBlock);
+        if (dtype != h->pending_dtype || kb_pending + kb_now > (int64_t(1) << 30)) {
+            st = flush_locked(h, s);
+            if (st != HESS_OK) return st;
+        }
+    }
+    h->pending.push_back({X, n_tokens, s});
+    h->pending_dtype = dtype;
+    h->pending_tokens += n_tokens;
+    h->N += n_tokens;
+    if (static_cast<int>(h->pending.size()) >= h->max_pending || h->pending_tokens >= h->flush_tokens)
+        return flush_locked(h, s);
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status hess_flush(hess_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    return flush_locked(h, static_cast<cudaStream_t>(stream));
+}
+
+HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_percent,
+                                         hess_stream_t stream, float* damp_value_out) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (!H_out) return fail(HESS_ERR_INVALID, "H_out is NULL");
+    if (reinterpret_cast<uintptr_t>(H_out) % 16 != 0) return fail(HESS_ERR_INVALID, "H_out is not 16-byte aligned");
+    if (!(damp_percent >= 0.0 && damp_percent < 1.0))
+        return fail(HESS_ERR_INVALID, "damp_percent must be in [0, 1)");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = flush_locked(h, s);
+    if (st != HESS_OK) return st;
+    if (h->N == 0) {
+        CUDA_TRY(cudaMemsetAsync(H_out, 0, static_cast<size_t>(h->d) * h->d * sizeof(float), s));
+        if (damp_value_out) {
+            *damp_value_out = 0.0f;
+            return read_status(h->status, s);
+        }
+        return HESS_OK;
+    }
+    const double scale = 2.0 / static_cast<double>(h->N);
+    CUDA_TRY(hk::launch_diag_damp(h->acc, static_cast<int>(h->d), h->T, scale, damp_percent,
+                                  h->damp64, h->damp32, s));
+    CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, h->damp64, s));
+    if (damp_value_out) {
+        float v = 0.0f;
+        CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
+        st = read_status(h->status, s);
+        if (st != HESS_OK) return st;
+        *damp_value_out = v;
+    }
+    return HESS_OK;
+}
+
+HESS_EXPORT int64_t hess_token_count(hess_t h) {
+    if (!h) return -1;
+    std::lock_guard<std::mutex> lk(h->mu);
+    return h->N;
+}
+
+HESS_EXPORT int64_t hess_pending_batches(hess_t h) {
+    if (!h) return -1;
+    std::lock_guard<std::mutex> lk(h->mu);
+    return static_cast<int64_t>(h->pending.size());
+}
+
+HESS_EXPORT int64_t hess_dim(hess_t h) { return h ? h->d : -1; }
+
+HESS_EXPORT hess_status hess_sync(hess_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    return read_status(h->status, static_cast<cudaStream_t>(stream));
+}
+
+HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->pending.clear();
+    h->pending_tokens = 0;
+    h->pending_dtype = -1;
+    h->N = 0;
+    CUDA_TRY(cudaMemsetAsync(h->acc, 0,
+                             static_cast<size_t>(h->n_tiles) * hk::kTileElems * sizeof(double), s));
+    CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status hess_set_option(hess_t h, int32_t option, int64_t value) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    switch (option) {
+        case HESS_OPT_FLUSH_TOKENS:
+            if (value < 1) return fail(HESS_ERR_INVALID, "flush_tokens must be >= 1");
+            h->flush_tokens = value;
+            return HESS_OK;
+        case HESS_OPT_MAX_PENDING:
+            if (value < 1 || value > hk::kMaxBatches)
+                return fail(HESS_ERR_INVALID, "max_pending must be in [1, %d]", hk::kMaxBatches);
+            h->max_pending = static_cast<int>(value);
+            return HESS_OK;
+        case HESS_OPT_CHUNK_TOKENS:
+            if (value < hk::kKBlock || value > 65536 || value % hk::kKBlock)
+                return fail(HESS_ERR_INVALID, "chunk_tokens must be a multiple of 64 in [64, 65536]");
+            h->chunk_tokens = static_cast<int>(value);
+            return HESS_OK;
+        case HESS_OPT_WAIT_TIMEOUT_NS:
+            if (value < 0) return fail(HESS_ERR_INVALID, "timeout must be >= 0");
+            h->timeout_ns = static_cast<unsigned long long>(value);
+            return HESS_OK;
+        case HESS_OPT_SPLIT_K:
+            if (value < 0 || value > 4096) return fail(HESS_ERR_INVALID, "split_k must be in [0, 4096]");
+            h->split_k = static_cast<int>(value);
+            return HESS_OK;
+        case HESS_OPT_GRID:
+            if (value < 0 || value > 65535) return fail(HESS_ERR_INVALID, "grid must be in [0, 65535]");
+            h->grid = static_cast<int>(value);
+            return HESS_OK;
+        default:
+            return fail(HESS_ERR_INVALID, "unknown option %d", option);
+    }
+}
+
+HESS_EXPORT hess_status hess_destroy(hess_t h) {
+    if (!h) return HESS_OK;
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(h->device);
+        cudaDeviceSynchronize();
+        cudaFree(h->acc);
+        cudaFree(h->status);
+        cudaFree(h->damp64);
+        cudaFree(h->damp32);
+        cudaEventDestroy(h->ev);
+        cudaSetDevice(cur);
+    }
+    delete h->params;
+    delete h;
+    return HESS_OK;
+}
+
+// ---------------------------------------------------------------- local H
+
+HESS_EXPORT hess_status local_hess_create(int64_t d, int32_t block, local_hess_t* out) {
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d <= 0) return fail(HESS_ERR_INVALID, "d must be positive");
+    if (block != 16) return fail(HESS_ERR_UNSUPPORTED, "block must be 16 (got %d)", block);
+    if (d % block != 0) return fail(HESS_ERR_UNSUPPORTED, "d %% block != 0");
+    if (d > (int64_t(1) << 20)) return fail(HESS_ERR_UNSUPPORTED, "d too large");
+    if (injected_alloc_failure()) return fail(HESS_ERR_OOM, "injected allocation failure (HESS_FAULT=alloc)");
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    hess_status st = prepare_device(dev);
+    if (st != HESS_OK) return st;
+    local_hess_ctx* h = new (std::nothrow) local_hess_ctx();
+    if (!h) return fail(HESS_ERR_OOM, "host allocation failed");
+    h->device = dev;
+    h->d = d;
+    h->block = block;
+    h->n_blocks = static_cast<int>(d / block);
+    const size_t bytes = static_cast<size_t>(h->n_blocks) * 256 * sizeof(double);
+    cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaMalloc(&h->acc, bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&h->status, 64);
+    if (e == cudaSuccess) e = cudaMemset(h->acc, 0, bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
+        cudaFree(h->acc);
+        cudaFree(h->status);
+        delete h;
+        return fail(s, "local_hess_create: %s", cudaGetErrorString(e));
+    }
+    *out = h;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status local_hess_add(local_hess_t h, const void* X, int64_t n_tokens, int64_t d,
+                                       int32_t block, int32_t dtype, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (n_tokens < 0) return fail(HESS_ERR_INVALID, "n_tokens < 0");
+    if (d != h->d) return fail(HESS_ERR_INVALID, "d = %lld does not match the handle (%lld)", (long long)d, (long long)h->d);
+    if (block != h->block) return fail(HESS_ERR_INVALID, "block does not match the handle");
+    if (dtype != HESS_BF16) {
+        if (dtype == HESS_F32) return fail(HESS_ERR_UNSUPPORTED, "local_hess_add takes bf16 input");
+        return fail(HESS_ERR_INVALID, "unknown dtype %d", dtype);
+    }
+    if (n_tokens == 0) return HESS_OK;
+    if (!X) return fail(HESS_ERR_INVALID, "X is NULL with n_tokens > 0");
+    if (reinterpret_cast<uintptr_t>(X) % 16 != 0) return fail(HESS_ERR_INVALID, "X is not 16-byte aligned");
+    if (n_tokens > (int64_t(1) << 31) - hk::kLocalKBlock) return fail(HESS_ERR_UNSUPPORTED, "n_tokens too large");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    hk::LocalParams p;
+    std::memset(&p, 0, sizeof(p));
+    st = encode_2d(&p.map, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->d, n_tokens, 64, hk::kLocalKBlock);
+    if (st != HESS_OK) return st;
+    p.acc = h->acc;
+    p.status = h->status;
+    p.timeout_ns = h->timeout_ns;
+    p.d = static_cast<int32_t>(h->d);
+    p.n_groups = static_cast<int32_t>(ceil_div(h->d, hk::kLocalGroup));
+    p.total_kb = static_cast<int32_t>(ceil_div(n_tokens, hk::kLocalKBlock));
+    const int64_t want = ceil_div(2 * static_cast<int64_t>(h->sm_count), p.n_groups);
+    p.n_ranges = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(want, p.total_kb)));
+    p.chunk_steps = 16;
+    const int64_t grid = static_cast<int64_t>(p.n_groups) * p.n_ranges;
+    if (grid > 0x7fffffff) return fail(HESS_ERR_UNSUPPORTED, "grid too large");
+    cudaError_t e = hk::launch_local_gram(p, static_cast<int>(grid), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(HESS_ERR_CUDA, "local launch failed: %s", cudaGetErrorString(e));
+    h->N += n_tokens;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status local_hess_read(local_hess_t h, float* out, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->N == 0) {
+        CUDA_TRY(cudaMemsetAsync(out, 0, static_cast<size_t>(h->n_blocks) * 256 * sizeof(float), s));
+        return HESS_OK;
+    }
+    CUDA_TRY(hk::launch_local_read(h->acc, out, h->n_blocks, 2.0 / static_cast<double>(h->N), s));
+    return HESS_OK;
+}
+
+HESS_EXPORT int64_t local_hess_token_count(local_hess_t h) {
+    if (!h) return -1;
+    std::lock_guard<std::mutex> lk(h->mu);
+    return h->N;
+}
+
+HESS_EXPORT hess_status local_hess_sync(local_hess_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    return read_status(h->status, static_cast<cudaStream_t>(stream));
+}
+
+HESS_EXPORT hess_status local_hess_reset(local_hess_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->N = 0;
+    CUDA_TRY(cudaMemsetAsync(h->acc, 0, static_cast<size_t>(h->n_blocks) * 256 * sizeof(double), s));
+    CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status local_hess_destroy(local_hess_t h) {
+    if (!h) return HESS_OK;
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(h->device);
+        cudaDeviceSynchronize();
+        cudaFree(h->acc);
+        cudaFree(h->status);
+        cudaSetDevice(cur);
+    }
+    delete h;
+    return HESS_OK;
+}
+
+HESS_EXPORT const char* hess_last_error(void) { return g_last_error.c_str(); }
+
+HESS_EXPORT int32_t hess_abi_version(void) { return HESS_ABI_VERSION; }

@@ -1,0 +1,85 @@
+// Parameter blocks and launchers shared by the host library and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace hk {
+
+// Edge of a tile of H (features).  The accumulator holds the upper-triangle
+// tiles (I <= J), tile-major, each tile column-major: element (r, c) of tile
+// t is acc[t * kTile * kTile + c * kTile + r].
+constexpr int kTile = 128;
+constexpr int kTileElems = kTile * kTile;
+// Tokens per pipeline stage ("k-block") of the SYRK kernels.
+constexpr int kKBlock = 64;
+// Batches one fused flush can hold; their tensor maps travel in the kernel
+// parameter block (up to 32 KB on sm_70 and later).
+constexpr int kMaxBatches = 192;
+
+// Device status word bits (OR-ed by kernels; read by hess_sync).
+constexpr uint32_t kStatusTimeoutLoad = 1u;
+constexpr uint32_t kStatusTimeoutMma = 2u;
+constexpr uint32_t kStatusTimeoutEpilogue = 4u;
+constexpr uint32_t kStatusTimeoutDrain = 8u;
+
+// One fused split-K pass over the queued batches of one dtype.
+struct SyrkParams {
+    CUtensorMap maps[kMaxBatches];      // batch b: dims {d, n_b}, 128B swizzle
+    int32_t kb_start[kMaxBatches + 1];  // prefix sum of ceil(n_b / kKBlock)
+    int32_t n_batches;
+    int32_t total_kb;       // k-blocks over all batches
+    int32_t n_slabs;        // token slabs (split-K factor)
+    int32_t n_tiles;        // upper-triangle tiles
+    int32_t tiles_per_dim;  // ceil(d / kTile)
+    int32_t chunk_kb;       // k-blocks per tensor-memory accumulation chain
+    int32_t d;
+    int32_t n_units;        // n_tiles * n_slabs
+    double* acc;            // fp64 accumulator (tile layout above)
+    uint32_t* status;
+    unsigned long long timeout_ns;
+};
+
+// Upper-triangle tile index of tile (I, J), I <= J < T (row-major over I).
+__host__ __device__ inline int tile_index(int I, int J, int T) {
+    return I * T - (I * (I - 1)) / 2 + (J - I);
+}
+
+size_t syrk_bf16_smem_bytes();
+cudaError_t syrk_bf16_prepare();  // sets the dynamic shared-memory limit (per device)
+cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s);
+
+size_t syrk_f32_smem_bytes();
+cudaError_t syrk_f32_prepare();
+cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
+
+// Materialize: damp = damp_percent * mean_i(acc_ii * scale) into damp_out
+// (fp64) and damp_out_f32; then H_out (row-major d x d fp32).
+cudaError_t launch_diag_damp(const double* acc, int d, int T, double scale, double damp_percent,
+                             double* damp_out, float* damp_out_f32, cudaStream_t s);
+cudaError_t launch_materialize(const double* acc, float* H_out, int d, int T, double scale,
+                               const double* damp, cudaStream_t s);
+
+// Local 16x16 block Grams.
+constexpr int kLocalKBlock = 64;   // tokens per stage
+constexpr int kLocalGroup = 256;   // features per CTA (16 blocks)
+struct LocalParams {
+    CUtensorMap map;        // X: dims {d, n}, box {64, kLocalKBlock}, 128B swizzle
+    double* acc;            // [d/16][16][16] fp64, full blocks
+    uint32_t* status;
+    unsigned long long timeout_ns;
+    int32_t d;
+    int32_t n_groups;       // ceil(d / kLocalGroup)
+    int32_t n_ranges;       // token ranges per group
+    int32_t total_kb;       // ceil(n / kLocalKBlock)
+    int32_t chunk_steps;    // 16-token MMA steps per register chain
+};
+size_t local_smem_bytes();
+cudaError_t local_prepare();
+cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
+cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
+                              cudaStream_t s);
+
+}  // namespace hk

@@ -1,0 +1,113 @@
+// Materialize kernels: scale the fp64 accumulator by 2/N, add the damping
+// term to the diagonal and write the full symmetric fp32 Hessian; and the
+// read-out of the local 16x16 block Hessians.
+//
+// GPTQModel wiki "QQQ", Concepts (Quadratic error compensation): the merged
+// Gram is scaled by 2 / total_samples, and the quantization pass adds
+// damp_percent * mean(diag(H)) to the diagonal (step 3); "Quantizer API and
+// results": the damping value handed back is that absolute amount.
+// GPTQModel PR #2979 Summary: N counts token vectors.
+//
+// Readings: the mean of the diagonal is taken of the scaled matrix, in
+// fp64; every output element is rounded once to fp32; H_out[j][i] is a copy
+// of H_out[i][j] (i <= j) so the result is exactly symmetric.
+#include "kernels.cuh"
+
+namespace hk {
+namespace {
+
+constexpr int kDiagThreads = 1024;
+
+__global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const double* __restrict__ acc, int d,
+                                                                 int T, double scale,
+                                                                 double damp_percent,
+                                                                 double* damp_out,
+                                                                 float* damp_out_f32) {
+    __shared__ double part[kDiagThreads / 32];
+    double s = 0.0;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const int ti = i / kTile, r = i % kTile;
+        s += acc[static_cast<size_t>(tile_index(ti, ti, T)) * kTileElems + r * kTile + r];
+    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        s = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.0;
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (threadIdx.x == 0) {
+            const double mean = (s * scale) / static_cast<double>(d);
+            const double damp = damp_percent * mean;
+            *damp_out = damp;
+            *damp_out_f32 = static_cast<float>(damp);
+        }
+    }
+}
+
+// One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter in
+// its stored (column-major) order and writes the mirrored rows of H_out;
+// pass 2 writes the direct rows through a shared-memory transpose.
+__global__ void __launch_bounds__(256) materialize_kernel(const double* __restrict__ acc,
+                                                          float* __restrict__ H, int d, int T,
+                                                          double scale,
+                                                          const double* __restrict__ damp_ptr) {
+    __shared__ float tr[64][65];
+    const int t = blockIdx.x;
+    const int a = blockIdx.y >> 1, b = blockIdx.y & 1;
+    int I = 0, rem = t;
+    while (rem >= T - I) {
+        rem -= T - I;
+        ++I;
+    }
+    const int J = I + rem;
+    if (I == J && a > b) return;  // lower quarter of a diagonal tile: covered by its mirror
+    const double damp = *damp_ptr;
+    const int r0 = I * kTile + a * 64, c0 = J * kTile + b * 64;
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+    const double* tile = acc + static_cast<size_t>(t) * kTileElems;
+    for (int cc = ty; cc < 64; cc += 4) {
+        const int r = r0 + tx, c = c0 + cc;
+        const double s = tile[(b * 64 + cc) * kTile + a * 64 + tx];
+        const float v = (r == c) ? static_cast<float>(s * scale + damp) : static_cast<float>(s * scale);
+        tr[cc][tx] = v;
+        if (r < d && c < d && r <= c) H[static_cast<size_t>(c) * d + r] = v;
+    }
+    __syncthreads();
+    for (int rr = ty; rr < 64; rr += 4) {
+        const int r = r0 + rr, c = c0 + tx;
+        if (r < d && c < d && r <= c) H[static_cast<size_t>(r) * d + c] = tr[tx][rr];
+    }
+}
+
+__global__ void __launch_bounds__(256) local_read_kernel(const double* __restrict__ acc,
+                                                         float* __restrict__ out, double scale) {
+    const int b = blockIdx.x;
+    const int i = threadIdx.x >> 4, j = threadIdx.x & 15;
+    const int lo = i < j ? i : j, hi = i < j ? j : i;
+    out[static_cast<size_t>(b) * 256 + threadIdx.x] =
+        static_cast<float>(acc[static_cast<size_t>(b) * 256 + lo * 16 + hi] * scale);
+}
+
+}  // namespace
+
+cudaError_t launch_diag_damp(const double* acc, int d, int T, double scale, double damp_percent,
+                             double* damp_out, float* damp_out_f32, cudaStream_t s) {
+    diag_damp_kernel<<<1, kDiagThreads, 0, s>>>(acc, d, T, scale, damp_percent, damp_out,
+                                                damp_out_f32);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_materialize(const double* acc, float* H_out, int d, int T, double scale,
+                               const double* damp, cudaStream_t s) {
+    const int n_tiles = T * (T + 1) / 2;
+    materialize_kernel<<<dim3(n_tiles, 4), 256, 0, s>>>(acc, H_out, d, T, scale, damp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
+                              cudaStream_t s) {
+    local_read_kernel<<<n_blocks, 256, 0, s>>>(acc, out, scale);
+    return cudaGetLastError();
+}
+
+}  // namespace hk

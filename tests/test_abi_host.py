@@ -1,0 +1,85 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function ``include/hess.h`` declares,
+and reject invalid arguments before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hess.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gptq_qqq_calibration_gb300 import build as b
+    b.build()
+    from gptq_qqq_calibration_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("hess_create", "hess_add_batch", "hess_materialize", "local_hess_add", "hess_destroy"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gptq_qqq_calibration_gb300 import _lib
+    names = declared_functions()
+    assert set(names) == set(_lib.PROTOTYPES), "binding prototypes and header disagree"
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version(lib):
+    text = open(HEADER).read()
+    v = int(re.search(r"#define HESS_ABI_VERSION (\d+)", text).group(1))
+    assert lib.hess_abi_version() == v
+
+
+def test_invalid_arguments_rejected_before_cuda(lib):
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_INVALID, HESS_ERR_UNSUPPORTED
+    h = ctypes.c_void_p()
+    assert lib.hess_create(0, ctypes.byref(h)) == HESS_ERR_INVALID
+    assert lib.hess_create(-8, ctypes.byref(h)) == HESS_ERR_INVALID
+    assert lib.hess_create(12, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED
+    assert b"multiple of 8" in lib.hess_last_error()
+    assert lib.hess_create(8, None) == HESS_ERR_INVALID
+    assert lib.hess_add_batch(None, None, 4, 0, None) == HESS_ERR_INVALID
+    assert lib.hess_flush(None, None) == HESS_ERR_INVALID
+    assert lib.hess_materialize(None, None, 0.01, None, None) == HESS_ERR_INVALID
+    assert lib.hess_set_option(None, 1, 5) == HESS_ERR_INVALID
+    assert lib.hess_token_count(None) == -1
+    assert lib.hess_destroy(None) == 0
+    assert lib.local_hess_create(64, 8, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED
+    assert lib.local_hess_create(40, 16, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED
+    assert lib.local_hess_add(None, None, 0, 16, 16, 0, None) == HESS_ERR_INVALID
+    assert lib.local_hess_destroy(None) == 0
+
+
+def test_injected_allocation_failure_reports_oom():
+    # In a child process so the environment knob stays local.
+    code = (
+        "import ctypes, sys; sys.path.insert(0, %r)\n"
+        "from gptq_qqq_calibration_gb300 import _lib\n"
+        "L = _lib.load(); h = ctypes.c_void_p()\n"
+        "assert L.hess_create(256, ctypes.byref(h)) == _lib.HESS_ERR_OOM\n"
+        "assert h.value is None\n"
+        "assert L.local_hess_create(256, 16, ctypes.byref(h)) == _lib.HESS_ERR_OOM\n"
+        "print('ok')\n" % ROOT)
+    env = dict(os.environ, HESS_FAULT="alloc")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stderr

@@ -1,0 +1,252 @@
+"""GPU parity of the CUDA path against the float64 oracle, small sizes.
+
+Every call goes through the C ABI (ctypes binding).  Sizes span several
+128x128 tiles, ragged token tails (n not a multiple of 64, n = 1), widths
+that are not multiples of the tile (136, 8), empty batches, several fused
+flushes, every split-K/chunk setting, and the degenerate N = 0 case.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL_BF16, batches, block_rel_err, host, rel_err
+from oracle import GramOracle, LocalGramOracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gptq_qqq_calibration_gb300 import build as b
+    b.build()
+
+
+def _run(d, counts, seed, damp=0.01, profile="normal", **opts):
+    from gptq_qqq_calibration_gb300 import Hessian
+    h = Hessian(d, **opts)
+    o = GramOracle(d)
+    for X in batches(d, counts, seed, profile):
+        h.add_batch(X)
+        o.add_batch(host(X))
+    H, dv = h.materialize(damp)
+    h.sync()
+    Href, dref = o.materialize(damp)
+    assert h.n_tokens == o.N
+    Hn = H.cpu().numpy()
+    h.close()
+    return Hn, dv, Href, dref
+
+
+@pytest.mark.parametrize("d,counts", [
+    (256, [128, 128, 128, 128]),
+    (136, [1, 63, 64, 65, 200]),
+    (8, [5, 70]),
+    (16, [1]),
+    (384, [333, 0, 1, 130]),
+    (640, [1000]),
+])
+def test_bf16_matches_oracle(d, counts):
+    H, dv, Href, dref = _run(d, counts, seed=d)
+    assert rel_err(H, Href) <= TOL_BF16
+    assert np.array_equal(H, H.T), "H_out must be bit-exactly symmetric"
+    assert dv == pytest.approx(dref, rel=1e-6)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(chunk_tokens=64), dict(chunk_tokens=128, split_k=3), dict(split_k=7),
+    dict(grid=5), dict(grid=1, chunk_tokens=64), dict(flush_tokens=1),
+    dict(max_pending=3, chunk_tokens=4096), dict(split_k=40),
+])
+def test_bf16_schedules(opts):
+    H, dv, Href, dref = _run(512, [700, 1, 64, 129, 512, 33], seed=11, **opts)
+    assert rel_err(H, Href) <= TOL_BF16
+    assert np.array_equal(H, H.T)
+
+
+def test_many_small_batches_fused_into_few_flushes():
+    rng = np.random.default_rng(5)
+    counts = rng.integers(1, 50, size=420)
+    H, dv, Href, dref = _run(256, counts, seed=12, damp=0.005)
+    assert rel_err(H, Href) <= TOL_BF16
+
+
+def test_outlier_channels():
+    H, dv, Href, dref = _run(768, [2000, 1500, 37], seed=13, profile="outlier")
+    assert rel_err(H, Href) <= TOL_BF16
+
+
+def test_empty_and_zero_tokens():
+    from gptq_qqq_calibration_gb300 import Hessian
+    h = Hessian(64)
+    h.add_batch(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"))
+    assert h.n_tokens == 0
+    H, dv = h.materialize(0.01)
+    assert dv == 0.0 and not torch.any(H)
+    X = torch.randn(10, 64, device="cuda").to(torch.bfloat16)
+    h.add_batch(X)
+    h.add_batch(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"))
+    assert h.n_tokens == 10
+    h.close()
+
+
+def test_materialize_is_not_destructive_and_reset_clears():
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 256
+    h = Hessian(d)
+    o = GramOracle(d)
+    for k, X in enumerate(batches(d, [100, 200, 300], 21)):
+        h.add_batch(X)
+        o.add_batch(host(X))
+        H, dv = h.materialize(0.01)
+        Href, dref = o.materialize(0.01)
+        assert rel_err(H.cpu().numpy(), Href) <= TOL_BF16
+    h.reset()
+    assert h.n_tokens == 0
+    X = next(batches(d, [77], 22))
+    h.add_batch(X)
+    o2 = GramOracle(d)
+    o2.add_batch(host(X))
+    H, _ = h.materialize(0.0)
+    assert rel_err(H.cpu().numpy(), o2.hessian()) <= TOL_BF16
+    h.close()
+
+
+def test_batches_from_another_stream():
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 256
+    h = Hessian(d)
+    o = GramOracle(d)
+    side = torch.cuda.Stream()
+    for k in range(6):
+        with torch.cuda.stream(side):
+            X = torch.randn(300 + k, d, device="cuda").to(torch.bfloat16)
+            h.add_batch(X, stream=side)
+        side.synchronize()
+        o.add_batch(host(X))
+    H, _ = h.materialize(0.0)
+    torch.cuda.synchronize()
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    h.close()
+
+
+def test_add_batch_allocates_no_device_memory():
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 1024
+    h = Hessian(d)
+    xs = [torch.randn(2000, d, device="cuda").to(torch.bfloat16) for _ in range(4)]
+    out = torch.empty((d, d), device="cuda")
+    h.add_batch(xs[0])
+    h.materialize(0.0, out=out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    a0 = torch.cuda.memory_allocated()
+    for X in xs:
+        h.add_batch(X)
+    h.flush()
+    h.materialize(0.01, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == a0
+    assert free1 == free0
+    h.close()
+
+
+def test_invalid_pointer_alignment_is_rejected():
+    from gptq_qqq_calibration_gb300 import _lib
+    L = _lib.load()
+    from gptq_qqq_calibration_gb300 import hess_create, hess_destroy
+    h = hess_create(64)
+    buf = torch.zeros(1024, dtype=torch.bfloat16, device="cuda")
+    assert L.hess_add_batch(h, buf.data_ptr() + 2, 4, 0, None) == _lib.HESS_ERR_INVALID
+    assert L.hess_add_batch(h, buf.data_ptr(), -1, 0, None) == _lib.HESS_ERR_INVALID
+    assert L.hess_add_batch(h, buf.data_ptr(), 4, 7, None) == _lib.HESS_ERR_INVALID
+    assert L.hess_token_count(h) == 0
+    hess_destroy(h)
+
+
+def test_device_wait_limit_reports_timeout_and_handle_recovers():
+    """A zero wait limit makes the kernel's first unsatisfied wait give up;
+    the kernel drains its copies, frees tensor memory and returns, and the
+    host reads HESS_ERR_TIMEOUT.  The handle then works again."""
+    from gptq_qqq_calibration_gb300 import Hessian, HessError
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_TIMEOUT
+    d = 512
+    h = Hessian(d, wait_timeout_ns=0)
+    X = torch.randn(4096, d, device="cuda").to(torch.bfloat16)
+    h.add_batch(X)
+    h.flush()
+    with pytest.raises(HessError) as ei:
+        h.sync()
+    assert ei.value.status == HESS_ERR_TIMEOUT
+    h.reset()
+    h.set_option("wait_timeout_ns", 2_000_000_000)
+    o = GramOracle(d)
+    h.add_batch(X)
+    o.add_batch(host(X))
+    H, _ = h.materialize(0.0)
+    h.sync()
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    h.close()
+
+
+# ------------------------------------------------------------------ local
+
+
+def _run_local(d, counts, seed, profile="normal"):
+    from gptq_qqq_calibration_gb300 import LocalHessian
+    lh = LocalHessian(d)
+    lo = LocalGramOracle(d)
+    for X in batches(d, counts, seed, profile):
+        lh.add_batch(X)
+        lo.add_batch(host(X))
+    L = lh.read()
+    lh.sync()
+    assert lh.n_tokens == lo.N
+    Ln = L.cpu().numpy()
+    lh.close()
+    return Ln, lo.read()
+
+
+@pytest.mark.parametrize("d,counts", [
+    (16, [1, 5]), (272, [63, 64, 65]), (512, [1000]), (4096, [257, 0, 31]), (1040, [2048, 3]),
+])
+def test_local_matches_oracle(d, counts):
+    L, Lref = _run_local(d, counts, seed=d + 1)
+    assert block_rel_err(L, Lref) <= TOL_BF16
+    assert np.array_equal(L, np.transpose(L, (0, 2, 1)))
+
+
+def test_local_heavy_tailed_channels():
+    L, Lref = _run_local(1024, [4096, 4096], seed=5, profile="student_t_every16")
+    assert block_rel_err(L, Lref) <= TOL_BF16
+
+
+def test_local_blocks_equal_diagonal_blocks_of_full_hessian():
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    d = 512
+    h, lh = Hessian(d), LocalHessian(d)
+    for X in batches(d, [900, 37], 31):
+        h.add_batch(X)
+        lh.add_batch(X)
+    H, _ = h.materialize(0.0)
+    L = lh.read().cpu().numpy()
+    H = H.cpu().numpy()
+    m = np.mean(np.diagonal(H))
+    for b in range(d // 16):
+        assert np.abs(L[b] - H[16 * b:16 * b + 16, 16 * b:16 * b + 16]).max() <= 2 * TOL_BF16 * m
+    h.close()
+    lh.close()
+
+
+def test_local_zero_and_reset():
+    from gptq_qqq_calibration_gb300 import LocalHessian
+    lh = LocalHessian(64)
+    assert not torch.any(lh.read())
+    lh.add_batch(torch.randn(10, 64, device="cuda").to(torch.bfloat16))
+    assert lh.n_tokens == 10
+    lh.reset()
+    assert lh.n_tokens == 0 and not torch.any(lh.read())
+    lh.close()
