@@ -54,7 +54,7 @@ class Clocks:
                 ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-i", str(self._index())],
+                 "--format=csv,noheader,nounits", "-lms", "20", "-i", str(self._index())],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -80,7 +80,7 @@ class Clocks:
             sm = [float(r[1]) for r in rows]
             mx = [float(r[2]) for r in rows]
             names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-            reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[4 + i]})
+            reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
             return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
                     "samples": len(rows)}
         except Exception as e:  # pragma: no cover
@@ -128,6 +128,8 @@ def run_ours(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
     wl = WORKLOADS[args.workload]
+    if args.batches:
+        wl = wl.scaled(n_batches=args.batches)
     d = wl.d
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
     n_tok = wl.n_tokens
@@ -149,6 +151,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as clk:
+        time.sleep(0.3)  # let the sampler start before the timed region
         e0.record()
         for _ in range(args.steps):
             step()
@@ -163,7 +166,7 @@ def run_ours(args):
     # call that triggered a flush (the GPU stays busy between them)
     kern = _time_syrk(h, xs, reps=3)
     syrk_tflops = flops / kern["seconds"] / 1e12
-    e2e = _e2e(h, wl, xs, d, args)
+    e2e = None if args.no_e2e else _e2e(h, wl, xs, d, args)
 
     res = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
@@ -413,10 +416,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="d4096_ragged360_loguniform")
+    ap.add_argument("--batches", type=int, default=0, help="use only the first K batches")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -127,7 +127,7 @@ struct hess_ctx {
     // options
     int64_t flush_tokens = 65536;
     int max_pending = hk::kMaxBatches;
-    int chunk_tokens = 1024;
+    int chunk_tokens = 256;
     unsigned long long timeout_ns = 2000000000ull;
     int split_k = 0;
     int grid = 0;
@@ -522,7 +522,7 @@ HESS_EXPORT hess_status local_hess_add(local_hess_t h, const void* X, int64_t n_
     p.total_kb = static_cast<int32_t>(ceil_div(n_tokens, hk::kLocalKBlock));
     const int64_t want = ceil_div(2 * static_cast<int64_t>(h->sm_count), p.n_groups);
     p.n_ranges = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(want, p.total_kb)));
-    p.chunk_steps = 16;
+    p.chunk_steps = 8;
     const int64_t grid = static_cast<int64_t>(p.n_groups) * p.n_ranges;
     if (grid > 0x7fffffff) return fail(HESS_ERR_UNSUPPORTED, "grid too large");
     cudaError_t e = hk::launch_local_gram(p, static_cast<int>(grid), static_cast<cudaStream_t>(stream));

@@ -15,13 +15,19 @@
 //     (128-byte swizzle) into a 6-deep shared-memory ring; on diagonal
 //     tiles A and B are the same slab and are loaded once;
 //   * warp 1 issues tcgen05.mma (M=128, N=128, K=16, both operands
-//     MN-major straight from the row-major X boxes) into one of two fp32
-//     tensor-memory accumulators; after `chunk_kb` k-blocks it hands the
-//     chain to the epilogue and continues in the other accumulator;
-//   * warps 2-5 fold each chain into an on-chip compensated sum (hi, lo) in
-//     tensor memory (TwoSum), so no fp32 chain runs longer than one chunk,
-//     and at the end of a unit add hi + lo in fp64 to the accumulator in
-//     global memory (red.add.f64; several slabs may add to one tile).
+//     MN-major straight from the row-major X boxes).  Consecutive 16-token
+//     steps alternate between two fp32 accumulator banks in tensor memory,
+//     and after `chunk_kb` k-blocks the pair is handed to the epilogue while
+//     the MMAs continue in a second pair (2 buffers x 2 banks x 128 columns);
+//   * warps 2-9 add the two banks and fold the chunk into a compensated
+//     (hi, lo) pair held in registers with an exact TwoSum on packed fp32
+//     pairs; at the end of a unit they add hi + lo in fp64 to the
+//     accumulator in global memory (red.add.f64, as several slabs may add
+//     to one tile).
+// Why the short chains: tcgen05 accumulation into tensor memory rounds
+// toward zero, so a chain of k MMA steps loses about k ulps of its running
+// sum (measured on GB300: relative bias -1.8e-6 at 1,024 tokens, -2.6e-4 at
+// 65,536).  Banks of 128 tokens keep that below 3e-7 of each entry.
 // Every mbarrier wait is bounded; on timeout a status bit is set, in-flight
 // copies and MMAs are drained, tensor memory is freed and the kernel returns.
 #include "kernels.cuh"
@@ -34,13 +40,13 @@ constexpr int kStages = 6;
 constexpr uint32_t kBoxBytes = 64 * 128;            // 64 tokens x 128 bytes
 constexpr uint32_t kOperandBytes = 2 * kBoxBytes;   // 128 features
 constexpr uint32_t kStageBytes = 2 * kOperandBytes; // A and B
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // acc0 | acc1 | hi | lo, 128 columns each
-constexpr uint32_t kColHi = 256, kColLo = 384;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 512;  // [buffer][bank] x 128 columns
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 128, 128);
-constexpr size_t kBarrierBytes = 8 * (2 * kStages + 5) + 16;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + kBarrierBytes;
+constexpr int kNumBarriers = 2 * kStages + 5;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + 8 * kNumBarriers + 16;
 
 struct Unit {
     int t, I, J, k0, k1;
@@ -62,13 +68,6 @@ __device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
     return un.k1 > un.k0;
 }
 
-__device__ __forceinline__ float two_sum(float a, float b, float& err) {
-    const float s = __fadd_rn(a, b);
-    const float bb = __fsub_rn(s, a);
-    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-    return s;
-}
-
 __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_constant__ SyrkParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -76,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
     uint8_t* const gbase = smem_raw + (base - raw);
     const uint32_t bar0 = base + kStages * kStageBytes;
     uint32_t* const tmem_slot =
-        reinterpret_cast<uint32_t*>(gbase + kStages * kStageBytes + 8 * (2 * kStages + 5));
+        reinterpret_cast<uint32_t*>(gbase + kStages * kStageBytes + 8 * kNumBarriers);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
@@ -93,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         fence_barrier_init();
@@ -176,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dt = tmem + static_cast<uint32_t>(ab) * 128u;
+                    const uint32_t dt = tmem + static_cast<uint32_t>(ab) * 256u;
                     for (int kb = c0; kb < c1; ++kb) {
                         if (!mbar_wait(full_bar(stage), phase, limit)) {
                             ok = false;
@@ -189,7 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                         for (int j = 0; j < kKBlock / 16; ++j) {
                             const uint64_t ad = smem_desc_sw128(sA + j * 2048u, kBoxBytes, 1024u);
                             const uint64_t bd = smem_desc_sw128(sB + j * 2048u, kBoxBytes, 1024u);
-                            umma_f16(dt, ad, bd, kIdesc, (kb > c0 || j > 0) ? 1u : 0u);
+                            // even steps -> bank 0, odd steps -> bank 1; each bank
+                            // starts afresh at the first step of the chunk
+                            umma_f16(dt + (j & 1) * 128u, ad, bd, kIdesc,
+                                     (kb > c0 || j > 1) ? 1u : 0u);
                         }
                         tc_commit(empty_bar(stage));
                         if (++stage == kStages) {
@@ -211,10 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
     } else {
-        // ------------------------------------------------ epilogue (4 warps)
-        const int q = warp & 3;  // tensor-memory lane quarter of this warp
+        // ------------------------------------------------ epilogue (8 warps)
+        // Warp w reads tensor-memory lanes 32*(w%4).. (its quarter) and one
+        // half of the 128 columns.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t col0 = static_cast<uint32_t>(half) * 64u;
+        uint64_t hi[32], lo[32];  // 64 columns of this thread's row, as pairs
         bool ok = true;
         int ab = 0;
         uint32_t aphase = 0;
@@ -222,17 +229,34 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             Unit un;
             if (!unit_at(p, u, un)) continue;
             const int nch = (un.k1 - un.k0 + p.chunk_kb - 1) / p.chunk_kb;
-            double* const out = p.acc + static_cast<size_t>(un.t) * kTileElems + row;
+            double* const out = p.acc + static_cast<size_t>(un.t) * kTileElems +
+                                static_cast<size_t>(col0) * kTile + row;
             for (int c = 0; c < nch; ++c) {
                 if (!mbar_wait(accf_bar(ab), aphase, limit)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t v[4][32];
-                const uint32_t ta = tmem + lane_off + static_cast<uint32_t>(ab) * 128u;
+                const uint32_t tb = tmem + lane_off + static_cast<uint32_t>(ab) * 256u + col0;
 #pragma unroll
-                for (int pc = 0; pc < 4; ++pc) tmem_ld32_sync(ta + pc * 32, v[pc]);
+                for (int it = 0; it < 8; ++it) {
+                    uint32_t b0[8], b1[8];
+                    tmem_ld8x2_sync(tb + it * 8, tb + 128 + it * 8, b0, b1);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t v = add2(pack2(b0[2 * k], b0[2 * k + 1]),
+                                                pack2(b1[2 * k], b1[2 * k + 1]));
+                        const int i = it * 4 + k;
+                        if (c == 0) {
+                            hi[i] = v;
+                            lo[i] = 0ull;
+                        } else {
+                            uint64_t e;
+                            hi[i] = two_sum2(hi[i], v, e);
+                            lo[i] = add2(lo[i], e);
+                        }
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce_bar(ab));
@@ -240,46 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                     ab = 0;
                     aphase ^= 1u;
                 }
-                const bool first = c == 0, last = c == nch - 1;
+            }
+            if (!ok) break;
 #pragma unroll
-                for (int pc = 0; pc < 4; ++pc) {
-                    const uint32_t th = tmem + lane_off + kColHi + pc * 32;
-                    const uint32_t tl = tmem + lane_off + kColLo + pc * 32;
-                    if (first && last) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            red_add_f64(out + (pc * 32 + k) * kTile,
-                                        static_cast<double>(__uint_as_float(v[pc][k])));
-                    } else if (first) {
-                        uint32_t z[32];
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) z[k] = 0u;
-                        tmem_st32_sync(th, v[pc]);
-                        tmem_st32_sync(tl, z);
-                    } else {
-                        uint32_t hi[32], lo[32];
-                        tmem_ld32_sync(th, hi);
-                        tmem_ld32_sync(tl, lo);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            float e;
-                            const float s =
-                                two_sum(__uint_as_float(hi[k]), __uint_as_float(v[pc][k]), e);
-                            hi[k] = __float_as_uint(s);
-                            lo[k] = __float_as_uint(__fadd_rn(__uint_as_float(lo[k]), e));
-                        }
-                        if (last) {
-#pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                red_add_f64(out + (pc * 32 + k) * kTile,
-                                            static_cast<double>(__uint_as_float(hi[k])) +
-                                                static_cast<double>(__uint_as_float(lo[k])));
-                        } else {
-                            tmem_st32_sync(th, hi);
-                            tmem_st32_sync(tl, lo);
-                        }
-                    }
-                }
+            for (int i = 0; i < 32; ++i) {
+                float h0, h1, l0, l1;
+                unpack2(hi[i], h0, h1);
+                unpack2(lo[i], l0, l1);
+                red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
+                red_add_f64(out + (2 * i + 1) * kTile,
+                            static_cast<double>(h1) + static_cast<double>(l1));
             }
         }
         if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);

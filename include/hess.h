@@ -74,9 +74,11 @@ typedef enum {
 typedef enum {
     HESS_OPT_FLUSH_TOKENS = 1,    /* pending tokens that trigger a flush (default 65536) */
     HESS_OPT_MAX_PENDING = 2,     /* pending batches that trigger a flush (1..192, default 192) */
-    HESS_OPT_CHUNK_TOKENS = 3,    /* tokens summed in one tensor-memory chain before the
-                                     compensated on-chip sum takes them (64..65536, multiple
-                                     of 64, default 1024) */
+    HESS_OPT_CHUNK_TOKENS = 3,    /* tokens per tensor-memory chunk before the compensated
+                                     on-chip sum takes it; each chunk alternates 16-token
+                                     steps between two chains (64..65536, multiple of 64,
+                                     default 256).  Tensor-core accumulation rounds toward
+                                     zero, so longer chunks bias H low. */
     HESS_OPT_WAIT_TIMEOUT_NS = 4, /* limit of every device-side wait, ns (default 2e9; 0 makes
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */

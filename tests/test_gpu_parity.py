@@ -52,7 +52,7 @@ def test_bf16_matches_oracle(d, counts):
     H, dv, Href, dref = _run(d, counts, seed=d)
     assert rel_err(H, Href) <= TOL_BF16
     assert np.array_equal(H, H.T), "H_out must be bit-exactly symmetric"
-    assert dv == pytest.approx(dref, rel=1e-6)
+    assert dv == pytest.approx(dref, rel=TOL_BF16)
 
 
 @pytest.mark.parametrize("opts", [
