@@ -42,6 +42,7 @@ PROTOTYPES = {
     "local_hess_sync": (_i32, [_vp, _vp]),
     "local_hess_reset": (_i32, [_vp, _vp]),
     "local_hess_destroy": (_i32, [_vp]),
+    "local_hess_compute_noalloc": (_i32, [_vp, _i64, _i64, _i32, _i32, _vp, _vp]),
     "hess_last_error": (ctypes.c_char_p, []),
     "hess_abi_version": (_i32, []),
 }

@@ -590,4 +590,8 @@ HESS_EXPORT hess_status local_hess_destroy(local_hess_t h) {
 
 HESS_EXPORT const char* hess_last_error(void) { return g_last_error.c_str(); }
 
+namespace hk {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace hk
+
 HESS_EXPORT int32_t hess_abi_version(void) { return HESS_ABI_VERSION; }

@@ -82,4 +82,7 @@ cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
                               cudaStream_t s);
 
+// Sets the thread-local message returned by hess_last_error().
+void set_last_error(const char* msg);
+
 }  // namespace hk

@@ -182,6 +182,31 @@ hess_status local_hess_sync(local_hess_t h, hess_stream_t stream);
 hess_status local_hess_reset(local_hess_t h, hess_stream_t stream);
 hess_status local_hess_destroy(local_hess_t h);
 
+/* One batch's local Hessian with no device allocation.  (No counterpart on
+ * the source pages: this is a library convenience.)
+ * For callers that must not allocate device memory while they run: those
+ * whose device memory is reserved up front by a pooling allocator, so that a
+ * cudaMalloc would fail or fragment the pool, and those whose runtime forbids
+ * the implicit synchronisation that cudaMalloc/cudaFree can cause.
+ *   out[b][i][j] = fp32(X_b^T X_b [i][j] * (2/n_tokens))  for this batch only,
+ *   the same values local_hess_create + local_hess_add + local_hess_read give
+ *   for a fresh handle; zeros when n_tokens == 0.
+ *   X     : device pointer, row-major [n_tokens, d] bf16, 16-byte aligned.
+ *   out   : device pointer, [d/16, 16, 16] fp32.
+ *   block : 16; dtype : HESS_BF16.
+ * Limit: d <= 16384 (the scratch holds 1,024 blocks); larger d gives
+ * HESS_ERR_UNSUPPORTED with a message naming the limit.
+ * Scratch: a 2 MiB fixed device array inside the library, held by every GPU
+ * that loads it until the process exits and shared by every call on that
+ * device.  Each call clears what it uses, but calls whose GPU work overlaps
+ * (unordered streams) race on it and give wrong results.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  The call is asynchronous on `stream`; a
+ * device-side wait that runs out leaves `out` invalid and is not reported. */
+hess_status local_hess_compute_noalloc(const void* X, int64_t n_tokens, int64_t d, int32_t block,
+                                       int32_t dtype, float* out, hess_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 
 /* Message of the last failed call on this thread ("" if none). */
