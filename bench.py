@@ -303,6 +303,28 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "frac": round(fl / t / 1e12 / bf16_burst, 4), "peak_source": "bf16_tflops (burst)"}}
     h.close()
     del xs
+    # fp32-input path on the ragged d = 4096 stream (split-tf32 kernel)
+    wl = WORKLOADS["d4096_ragged360_loguniform"]
+    xs = [wl.batch(b, device="cuda", dtype=torch.float32) for b in range(len(wl.token_counts))]
+    h = Hessian(wl.d)
+    for _ in range(2):
+        h.reset()
+        for X in xs:
+            h.add_batch(X)
+        h.flush()
+    torch.cuda.synchronize()
+    kern = _time_syrk(h, xs, reps=2)
+    fl = algo_flops(wl.n_tokens, wl.d)
+    t = kern["seconds"]
+    tf32_peak = bf16_burst / 2.0  # dense tf32 runs at half the bf16 rate
+    out["f32_input_ragged"] = {
+        "workload": wl.name + " (fp32 input)", "tflops": round(fl / t / 1e12, 2), "ms": round(t * 1e3, 3),
+        "tokens_per_s": round(wl.n_tokens / t, 1), "mma_per_8_tokens": 3,
+        "roofline": {"bound": "tensor", "achieved_tf32": round(3 * fl / t / 1e12, 2), "peak": tf32_peak,
+                     "unit": "TFLOP/s", "frac": round(3 * fl / t / 1e12 / tf32_peak, 4),
+                     "peak_source": "bf16_tflops (burst) x 1/2 (nominal tf32:bf16 ratio)"}}
+    h.close()
+    del xs
     # local_hessian: 8 updates of 32768 tokens at d = 4096
     wl = WORKLOADS["local_d4096_8x32768"]
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]

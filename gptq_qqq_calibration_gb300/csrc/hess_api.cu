@@ -192,21 +192,25 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     const bool f32 = h->pending_dtype == HESS_F32;
     const int nb = static_cast<int>(h->pending.size());
     p.kb_start[0] = 0;
+    const int kblock = f32 ? hk::kKBlockF32 : hk::kKBlock;
     for (int b = 0; b < nb; ++b) {
         const auto& q = h->pending[b];
         hess_status st =
             f32 ? encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, h->d, q.n, 32,
-                            hk::kKBlock)
+                            hk::kKBlockF32)
                 : encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->d, q.n, 64,
                             hk::kKBlock);
         if (st != HESS_OK) return st;
-        p.kb_start[b + 1] = p.kb_start[b] + static_cast<int32_t>(ceil_div(q.n, hk::kKBlock));
+        p.kb_start[b + 1] = p.kb_start[b] + static_cast<int32_t>(ceil_div(q.n, kblock));
     }
     p.n_batches = nb;
     p.total_kb = p.kb_start[nb];
     p.n_tiles = h->n_tiles;
     p.tiles_per_dim = h->T;
-    p.chunk_kb = std::max(1, h->chunk_tokens / hk::kKBlock);
+    // fp32 input runs three MMAs per 8 tokens (hi*hi plus two cross terms), so
+    // its chains are 4x shorter in tokens for the same rounding bias.
+    p.chunk_kb = f32 ? std::max(1, h->chunk_tokens / 4 / hk::kKBlockF32)
+                     : std::max(1, h->chunk_tokens / hk::kKBlock);
     p.d = static_cast<int32_t>(h->d);
     p.acc = h->acc;
     p.status = h->status;

@@ -15,6 +15,8 @@ constexpr int kTile = 128;
 constexpr int kTileElems = kTile * kTile;
 // Tokens per pipeline stage ("k-block") of the SYRK kernels.
 constexpr int kKBlock = 64;
+// Tokens per k-block of the fp32-input SYRK kernel.
+constexpr int kKBlockF32 = 32;
 // Batches one fused flush can hold; their tensor maps travel in the kernel
 // parameter block (up to 32 KB on sm_70 and later).
 constexpr int kMaxBatches = 192;

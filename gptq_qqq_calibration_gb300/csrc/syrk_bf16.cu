@@ -30,43 +30,25 @@
 // 65,536).  Banks of 128 tokens keep that below 3e-7 of each entry.
 // Every mbarrier wait is bounded; on timeout a status bit is set, in-flight
 // copies and MMAs are drained, tensor memory is freed and the kernel returns.
-#include "kernels.cuh"
-#include "ptx.cuh"
+#include "syrk_common.cuh"
 
 namespace hk {
 namespace {
+
+using syrk::Unit;
+using syrk::unit_at;
+using syrk::kEpiWarps;
+using syrk::kDrainLimitNs;
 
 constexpr int kStages = 6;
 constexpr uint32_t kBoxBytes = 64 * 128;            // 64 tokens x 128 bytes
 constexpr uint32_t kOperandBytes = 2 * kBoxBytes;   // 128 features
 constexpr uint32_t kStageBytes = 2 * kOperandBytes; // A and B
-constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;  // [buffer][bank] x 128 columns
-constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 128, 128);
 constexpr int kNumBarriers = 2 * kStages + 5;
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + 8 * kNumBarriers + 16;
-
-struct Unit {
-    int t, I, J, k0, k1;
-};
-
-__device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
-    const int slab = u / p.n_tiles;
-    const int t = u - slab * p.n_tiles;
-    int i = 0, rem = t;
-    while (rem >= p.tiles_per_dim - i) {
-        rem -= p.tiles_per_dim - i;
-        ++i;
-    }
-    un.t = t;
-    un.I = i;
-    un.J = i + rem;
-    un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
-    un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
-    return un.k1 > un.k0;
-}
 
 __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_constant__ SyrkParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -214,69 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
-        // Warp w reads tensor-memory lanes 32*(w%4).. (its quarter) and one
-        // half of the 128 columns.
-        const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
-        const int row = q * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t col0 = static_cast<uint32_t>(half) * 64u;
-        uint64_t hi[32], lo[32];  // 64 columns of this thread's row, as pairs
-        bool ok = true;
-        int ab = 0;
-        uint32_t aphase = 0;
-        for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-            Unit un;
-            if (!unit_at(p, u, un)) continue;
-            const int nch = (un.k1 - un.k0 + p.chunk_kb - 1) / p.chunk_kb;
-            double* const out = p.acc + static_cast<size_t>(un.t) * kTileElems +
-                                static_cast<size_t>(col0) * kTile + row;
-            for (int c = 0; c < nch; ++c) {
-                if (!mbar_wait(accf_bar(ab), aphase, limit)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tb = tmem + lane_off + static_cast<uint32_t>(ab) * 256u + col0;
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    uint32_t b0[8], b1[8];
-                    tmem_ld8x2_sync(tb + it * 8, tb + 128 + it * 8, b0, b1);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t v = add2(pack2(b0[2 * k], b0[2 * k + 1]),
-                                                pack2(b1[2 * k], b1[2 * k + 1]));
-                        const int i = it * 4 + k;
-                        if (c == 0) {
-                            hi[i] = v;
-                            lo[i] = 0ull;
-                        } else {
-                            uint64_t e;
-                            hi[i] = two_sum2(hi[i], v, e);
-                            lo[i] = add2(lo[i], e);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce_bar(ab));
-                if (++ab == 2) {
-                    ab = 0;
-                    aphase ^= 1u;
-                }
-            }
-            if (!ok) break;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float h0, h1, l0, l1;
-                unpack2(hi[i], h0, h1);
-                unpack2(lo[i], l0, l1);
-                red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
-                red_add_f64(out + (2 * i + 1) * kTile,
-                            static_cast<double>(h1) + static_cast<double>(l1));
-            }
-        }
-        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);
+        syrk::epilogue(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
     }
 
     tc_fence_before();

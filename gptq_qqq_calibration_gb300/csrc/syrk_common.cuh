@@ -1,0 +1,109 @@
+// Pieces shared by the bf16 and fp32 SYRK kernels: the unit schedule and
+// the compensated epilogue that folds tensor-memory chunks into registers.
+#pragma once
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace hk {
+namespace syrk {
+
+// A unit is one 128x128 upper tile (I, J) over one slab [k0, k1) of the
+// flush's k-blocks.  Units are numbered slab-major so that the CTAs running
+// at the same time stream the same tokens.
+struct Unit {
+    int t, I, J, k0, k1;
+};
+
+__device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
+    const int slab = u / p.n_tiles;
+    const int t = u - slab * p.n_tiles;
+    int i = 0, rem = t;
+    while (rem >= p.tiles_per_dim - i) {
+        rem -= p.tiles_per_dim - i;
+        ++i;
+    }
+    un.t = t;
+    un.I = i;
+    un.J = i + rem;
+    un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
+    un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
+    return un.k1 > un.k0;
+}
+
+constexpr int kEpiWarps = 8;
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+
+// Epilogue of one CTA (8 warps, warps first_warp .. first_warp + 7).
+// Tensor memory holds 2 buffers x 2 banks x 128 columns; chunk c of a unit
+// sits in buffer (chunk counter & 1).  Each warp reads its lane quarter
+// (warp % 4) and one half of the columns, adds the two banks, and folds the
+// sum into a (hi, lo) pair with an exact TwoSum on packed fp32 pairs.  At the
+// end of a unit, hi + lo is added in fp64 to the accumulator.
+__device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int warp, int lane,
+                                         int first_warp, uint32_t accf_bar0, uint32_t acce_bar0,
+                                         unsigned long long limit) {
+    const int q = warp & 3;
+    const int half = (warp - first_warp) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half) * 64u;
+    uint64_t hi[32], lo[32];  // 64 columns of this thread's row, as pairs
+    bool ok = true;
+    int ab = 0;
+    uint32_t aphase = 0;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        Unit un;
+        if (!unit_at(p, u, un)) continue;
+        const int nch = (un.k1 - un.k0 + p.chunk_kb - 1) / p.chunk_kb;
+        double* const out = p.acc + static_cast<size_t>(un.t) * kTileElems +
+                            static_cast<size_t>(col0) * kTile + row;
+        for (int c = 0; c < nch; ++c) {
+            if (!mbar_wait(accf_bar0 + 8u * ab, aphase, limit)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem + lane_off + static_cast<uint32_t>(ab) * 256u + col0;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                uint32_t b0[8], b1[8];
+                tmem_ld8x2_sync(tb + it * 8, tb + 128 + it * 8, b0, b1);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t v = add2(pack2(b0[2 * k], b0[2 * k + 1]),
+                                            pack2(b1[2 * k], b1[2 * k + 1]));
+                    const int i = it * 4 + k;
+                    if (c == 0) {
+                        hi[i] = v;
+                        lo[i] = 0ull;
+                    } else {
+                        uint64_t e;
+                        hi[i] = two_sum2(hi[i], v, e);
+                        lo[i] = add2(lo[i], e);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar0 + 8u * ab);
+            if (++ab == 2) {
+                ab = 0;
+                aphase ^= 1u;
+            }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float h0, h1, l0, l1;
+            unpack2(hi[i], h0, h1);
+            unpack2(lo[i], l0, l1);
+            red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
+            red_add_f64(out + (2 * i + 1) * kTile, static_cast<double>(h1) + static_cast<double>(l1));
+        }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);
+}
+
+}  // namespace syrk
+}  // namespace hk

@@ -1,11 +1,291 @@
-// fp32-input SYRK (placeholder until the split-TF32 kernel lands): every
-// launch reports cudaErrorNotSupported, which the host maps to an error.
-#include "kernels.cuh"
+// Symmetric rank-k update S += X^T X for fp32 activations on sm_103a.
+//
+// The pages' fp32 option copies each batch to float32 and runs a float32
+// GEMM on CUDA cores (NVIDIA Model-Optimizer PR #3002, "What does this PR
+// do?").  Here the same sums run on the tensor cores with a split that keeps
+// fp32 accuracy: every value is written x = hi + lo, hi = x rounded to
+// nearest tf32 (11 significant bits) and lo = x - hi (exact), and
+//     x_i x_j ~= hi_i hi_j + (hi_i lo_j + lo_i hi_j)
+// which drops only lo_i lo_j (relative <= 2^-22, zero mean because the
+// rounding is to nearest) and the tf32 truncation of lo (relative 2^-22).
+//
+// How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
+//   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
+//     128-byte swizzle) into a 3-deep landing ring; the whole of warp 0 then
+//     converts each landed stage into hi / lo planes of a 2-deep MMA ring,
+//     at the same byte offsets (so the swizzle carries over), and refills
+//     the landing slot at once;
+//   * warp 1 issues tcgen05.mma kind::tf32 (M=N=128, K=8): hi*hi into bank 0
+//     and the two cross terms into bank 1, so the small cross terms never
+//     ride on the large running sum;
+//   * warps 2-9 run the shared compensated epilogue (bank 0 + bank 1 folded
+//     into registers by TwoSum, fp64 add at the end of a unit).
+// Tensor-core accumulation rounds toward zero, so chunks are short (64
+// tokens by default: 8 hi*hi steps).  Every wait is bounded.
+#include "syrk_common.cuh"
 
 namespace hk {
+namespace {
 
-size_t syrk_f32_smem_bytes() { return 0; }
-cudaError_t syrk_f32_prepare() { return cudaSuccess; }
-cudaError_t launch_syrk_f32(const SyrkParams&, int, cudaStream_t) { return cudaErrorNotSupported; }
+using syrk::kDrainLimitNs;
+using syrk::kEpiWarps;
+using syrk::Unit;
+using syrk::unit_at;
+
+constexpr int kKB = kKBlockF32;                     // tokens per k-block
+constexpr int kLand = 3;                            // landing stages
+constexpr int kCvt = 2;                             // converted stages
+constexpr uint32_t kBoxBytes = kKB * 128;           // 32 tokens x 32 fp32
+constexpr uint32_t kOpBytes = 4 * kBoxBytes;        // 128 features
+constexpr uint32_t kLandBytes = 2 * kOpBytes;       // A | B raw
+constexpr uint32_t kCvtBytes = 4 * kOpBytes;        // A hi | A lo | B hi | B lo
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = instr_desc_mn_major(2u /*tf32*/, 128, 128);
+constexpr int kNumBarriers = 2 * kLand + 2 * kCvt + 5;
+constexpr uint32_t kCvtBase = kLand * kLandBytes;
+constexpr size_t kSmemBytes =
+    1024 + kLand * kLandBytes + kCvt * kCvtBytes + 8 * kNumBarriers + 16;
+
+// Walks the (unit, k-block) sequence of this CTA.
+struct Cursor {
+    int u;
+    Unit un;
+    int kb;
+    int b;  // batch holding kb
+    bool valid;
+};
+
+__device__ __forceinline__ void cursor_seek(const SyrkParams& p, Cursor& c) {
+    while (c.u < p.n_units) {
+        if (unit_at(p, c.u, c.un)) {
+            c.kb = c.un.k0;
+            c.b = 0;
+            while (p.kb_start[c.b + 1] <= c.kb) ++c.b;
+            c.valid = true;
+            return;
+        }
+        c.u += gridDim.x;
+    }
+    c.valid = false;
+}
+
+__device__ __forceinline__ void cursor_start(const SyrkParams& p, Cursor& c) {
+    c.u = blockIdx.x;
+    cursor_seek(p, c);
+}
+
+__device__ __forceinline__ void cursor_next(const SyrkParams& p, Cursor& c) {
+    if (++c.kb < c.un.k1) {
+        while (p.kb_start[c.b + 1] <= c.kb) ++c.b;
+        return;
+    }
+    c.u += gridDim.x;
+    cursor_seek(p, c);
+}
+
+// hi = x rounded to nearest tf32 (low 13 bits cleared), lo = x - hi exactly.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    const uint32_t u = __float_as_uint(x);
+    hi = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
+    lo = __fsub_rn(x, hi);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_constant__ SyrkParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + kLand * kLandBytes + kCvt * kCvtBytes;
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(
+        gbase + kLand * kLandBytes + kCvt * kCvtBytes + 8 * kNumBarriers);
+    auto land_full = [&](int s) { return bar0 + 8u * s; };
+    auto cvt_full = [&](int s) { return bar0 + 8u * (kLand + s); };
+    auto cvt_empty = [&](int s) { return bar0 + 8u * (kLand + kCvt + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (kLand + 2 * kCvt + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (kLand + 2 * kCvt + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (kLand + 2 * kCvt + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kLand; ++s) mbar_init(land_full(s), 1);
+        for (int s = 0; s < kCvt; ++s) {
+            mbar_init(cvt_full(s), 1);
+            mbar_init(cvt_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const unsigned long long limit = p.timeout_ns;
+
+    if (warp == 0) {
+        // ---------------------------------- TMA producer + tf32 splitter
+        bool ok = true;
+        Cursor L, C;
+        cursor_start(p, L);
+        cursor_start(p, C);
+        uint32_t issued = 0, converted = 0;
+        auto issue = [&]() {
+            const int s = issued % kLand;
+            const bool diag = L.un.I == L.un.J;
+            if (lane == 0) {
+                const CUtensorMap* m = &p.maps[L.b];
+                const int tok = (L.kb - p.kb_start[L.b]) * kKB;
+                const uint32_t dst = base + s * kLandBytes;
+                mbar_arrive_expect_tx(land_full(s), diag ? kOpBytes : kLandBytes);
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, m, land_full(s), L.un.I * kTile + 32 * bx, tok);
+                if (!diag)
+                    for (int bx = 0; bx < 4; ++bx)
+                        tma_load_2d(dst + kOpBytes + bx * kBoxBytes, m, land_full(s),
+                                    L.un.J * kTile + 32 * bx, tok);
+            }
+            ++issued;
+            cursor_next(p, L);
+        };
+        while (L.valid && issued < static_cast<uint32_t>(kLand)) issue();
+        while (ok && C.valid) {
+            const int s = converted % kLand;
+            const int c = converted % kCvt;
+            if (!mbar_wait(land_full(s), (converted / kLand) & 1u, limit) ||
+                !mbar_wait(cvt_empty(c), ((converted / kCvt) & 1u) ^ 1u, limit)) {
+                ok = false;
+                break;
+            }
+            const bool diag = C.un.I == C.un.J;
+            const int n_ops = diag ? 1 : 2;
+            const float4* src = reinterpret_cast<const float4*>(gbase + s * kLandBytes);
+            uint8_t* const dst = gbase + kCvtBase + c * kCvtBytes;
+            for (int op = 0; op < n_ops; ++op) {
+                float4* hi_p = reinterpret_cast<float4*>(dst + op * 2 * kOpBytes);
+                float4* lo_p = reinterpret_cast<float4*>(dst + op * 2 * kOpBytes + kOpBytes);
+                const float4* sp = src + op * (kOpBytes / 16);
+#pragma unroll 8
+                for (int i = lane; i < static_cast<int>(kOpBytes / 16); i += 32) {
+                    const float4 x = sp[i];
+                    float4 h, l;
+                    split_tf32(x.x, h.x, l.x);
+                    split_tf32(x.y, h.y, l.y);
+                    split_tf32(x.z, h.z, l.z);
+                    split_tf32(x.w, h.w, l.w);
+                    hi_p[i] = h;
+                    lo_p[i] = l;
+                }
+            }
+            // generic-proxy writes (and reads of the landing slot) must be
+            // visible to / ordered before the async proxy (MMA, next TMA)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cvt_full(c));
+            ++converted;
+            cursor_next(p, C);
+            if (L.valid) issue();
+        }
+        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
+        // Every issued copy must land before the CTA may exit.
+        if (lane == 0) {
+            for (uint32_t k = converted; k < issued; ++k) {
+                if (!mbar_wait(land_full(k % kLand), (k / kLand) & 1u, kDrainLimitNs)) {
+                    atomicOr(p.status, kStatusTimeoutDrain);
+                    break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t consumed = 0;
+            int ab = 0;
+            uint32_t aphase = 0;
+            for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+                Unit un;
+                if (!unit_at(p, u, un)) continue;
+                const bool diag = un.I == un.J;
+                for (int c0 = un.k0; c0 < un.k1; c0 += p.chunk_kb) {
+                    const int c1 = min(c0 + p.chunk_kb, un.k1);
+                    if (!mbar_wait(acce_bar(ab), aphase ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d0 = tmem + static_cast<uint32_t>(ab) * 256u;
+                    const uint32_t d1 = d0 + 128u;
+                    for (int kb = c0; kb < c1; ++kb) {
+                        const int cs = consumed % kCvt;
+                        if (!mbar_wait(cvt_full(cs), (consumed / kCvt) & 1u, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sA = base + kCvtBase + cs * kCvtBytes;
+                        const uint32_t sB = diag ? sA : sA + 2 * kOpBytes;
+#pragma unroll
+                        for (int j = 0; j < kKB / 8; ++j) {
+                            const uint32_t off = j * 1024u;
+                            const uint64_t ahi = smem_desc_sw128(sA + off, kBoxBytes, 1024u);
+                            const uint64_t alo = smem_desc_sw128(sA + kOpBytes + off, kBoxBytes, 1024u);
+                            const uint64_t bhi = smem_desc_sw128(sB + off, kBoxBytes, 1024u);
+                            const uint64_t blo = smem_desc_sw128(sB + kOpBytes + off, kBoxBytes, 1024u);
+                            const uint32_t acc = (kb > c0 || j > 0) ? 1u : 0u;
+                            umma_tf32(d0, ahi, bhi, kIdesc, acc);
+                            umma_tf32(d1, ahi, blo, kIdesc, acc);
+                            umma_tf32(d1, alo, bhi, kIdesc, 1u);
+                        }
+                        tc_commit(cvt_empty(cs));
+                        ++consumed;
+                    }
+                    if (!ok) break;
+                    tc_commit(accf_bar(ab));
+                    if (++ab == 2) {
+                        ab = 0;
+                        aphase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutMma);
+            tc_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (8 warps)
+        syrk::epilogue(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t syrk_f32_smem_bytes() { return kSmemBytes; }
+
+cudaError_t syrk_f32_prepare() {
+    return cudaFuncSetAttribute(syrk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes));
+}
+
+cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s) {
+    syrk_f32_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
 
 }  // namespace hk

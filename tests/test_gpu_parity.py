@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL_BF16, batches, block_rel_err, host, rel_err
+from helpers import TOL_BF16, TOL_F32, batches, block_rel_err, host, rel_err
 from oracle import GramOracle, LocalGramOracle
 
 pytestmark = pytest.mark.gpu
@@ -24,11 +24,11 @@ def _built():
     b.build()
 
 
-def _run(d, counts, seed, damp=0.01, profile="normal", **opts):
+def _run(d, counts, seed, damp=0.01, profile="normal", dtype=torch.bfloat16, **opts):
     from gptq_qqq_calibration_gb300 import Hessian
     h = Hessian(d, **opts)
     o = GramOracle(d)
-    for X in batches(d, counts, seed, profile):
+    for X in batches(d, counts, seed, profile, dtype=dtype):
         h.add_batch(X)
         o.add_batch(host(X))
     H, dv = h.materialize(damp)
@@ -64,6 +64,71 @@ def test_bf16_schedules(opts):
     H, dv, Href, dref = _run(512, [700, 1, 64, 129, 512, 33], seed=11, **opts)
     assert rel_err(H, Href) <= TOL_BF16
     assert np.array_equal(H, H.T)
+
+
+@pytest.mark.parametrize("d,counts", [
+    (256, [128, 128, 128, 128]),
+    (136, [1, 31, 32, 33, 200]),
+    (8, [5, 70]),
+    (384, [333, 0, 1, 130]),
+    (640, [1000, 77]),
+])
+def test_f32_matches_oracle(d, counts):
+    H, dv, Href, dref = _run(d, counts, seed=d + 7, dtype=torch.float32)
+    assert rel_err(H, Href) <= TOL_F32
+    assert np.array_equal(H, H.T)
+    assert dv == pytest.approx(dref, rel=TOL_F32)
+
+
+@pytest.mark.parametrize("opts", [dict(chunk_tokens=128), dict(split_k=5), dict(grid=3),
+                                  dict(flush_tokens=1), dict(chunk_tokens=2048)])
+def test_f32_schedules(opts):
+    H, dv, Href, dref = _run(512, [700, 1, 32, 129, 512, 33], seed=17, dtype=torch.float32, **opts)
+    assert rel_err(H, Href) <= TOL_F32
+
+
+def test_f32_outlier_and_loguniform_channels():
+    H, _, Href, _ = _run(768, [2000, 1500, 37], seed=19, profile="outlier", dtype=torch.float32)
+    assert rel_err(H, Href) <= TOL_F32
+    H, _, Href, _ = _run(512, [2000, 999], seed=20, profile="loguniform", dtype=torch.float32)
+    assert rel_err(H, Href) <= TOL_F32
+
+
+def test_mixed_dtypes_in_one_handle():
+    """bf16 and fp32 batches may alternate; a dtype switch flushes (H is fp32
+    either way, Model-Optimizer PR #3002)."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 384
+    h = Hessian(d)
+    o = GramOracle(d)
+    for k, n in enumerate((300, 17, 1000, 64)):
+        dt = torch.bfloat16 if k % 2 == 0 else torch.float32
+        X = next(batches(d, [n], 40 + k, dtype=dt))
+        h.add_batch(X)
+        o.add_batch(host(X))
+    H, _ = h.materialize(0.0)
+    h.sync()
+    assert h.n_tokens == o.N
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    h.close()
+
+
+def test_f32_path_on_upcast_bf16_equals_bf16_path():
+    """bf16 -> fp32 is exact, so both kernels see the same numbers."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 512
+    xs = list(batches(d, [900, 33, 1200], 41))
+    hb, hf = Hessian(d), Hessian(d)
+    for X in xs:
+        hb.add_batch(X)
+        hf.add_batch(X.float())
+    Hb, _ = hb.materialize(0.0)
+    Hf, _ = hf.materialize(0.0)
+    torch.cuda.synchronize()
+    m = float(torch.diagonal(Hf).mean())
+    assert float((Hb - Hf).abs().max()) <= TOL_BF16 * m
+    hb.close()
+    hf.close()
 
 
 def test_many_small_batches_fused_into_few_flushes():

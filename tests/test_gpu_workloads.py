@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL_BF16, block_rel_err, host
+from helpers import TOL_BF16, TOL_F32, block_rel_err, host
 from oracle import GramOracle, LocalGramOracle, column_sum_of_squares, gram_columns
 
 pytestmark = [pytest.mark.gpu]
@@ -46,7 +46,7 @@ def test_d256_four_batches_full_oracle():
     h.close()
 
 
-def _sampled_check(name, n_cols=48, **opts):
+def _sampled_check(name, n_cols=48, dtype=torch.bfloat16, **opts):
     from gptq_qqq_calibration_gb300 import Hessian
     from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
     wl = WORKLOADS[name]
@@ -57,7 +57,7 @@ def _sampled_check(name, n_cols=48, **opts):
     sq = np.zeros(d)
     N = 0
     for b in range(len(wl.token_counts)):
-        X = wl.batch(b, device="cuda")
+        X = wl.batch(b, device="cuda", dtype=dtype)
         h.add_batch(X)
         Xh = host(X)
         part, n = gram_columns([Xh], cols)
@@ -73,7 +73,8 @@ def _sampled_check(name, n_cols=48, **opts):
     ref[cols, np.arange(n_cols)] += wl.damp_percent * mean_diag
     got = H[:, torch.from_numpy(cols).cuda()].cpu().numpy().astype(np.float64)
     err = np.abs(got - ref).max() / mean_diag
-    assert damp == pytest.approx(wl.damp_percent * mean_diag, rel=TOL_BF16)
+    assert damp == pytest.approx(wl.damp_percent * mean_diag,
+                                 rel=TOL_F32 if dtype == torch.float32 else TOL_BF16)
     rows = H[torch.from_numpy(cols).cuda(), :].cpu().numpy()
     assert np.array_equal(rows.T, got.astype(np.float32))
     h.close()
@@ -88,6 +89,11 @@ def test_d2560_ragged_outlier_channels():
 def test_d4096_ragged_loguniform_bf16():
     err = _sampled_check("d4096_ragged360_loguniform")
     assert err <= TOL_BF16, err
+
+
+def test_d4096_ragged_loguniform_f32():
+    err = _sampled_check("d4096_ragged360_loguniform", dtype=torch.float32)
+    assert err <= TOL_F32, err
 
 
 def test_d4096_large_batches():
