@@ -64,7 +64,8 @@ EncodeTiledFn encode_fn() {
 // 2-D row-major [rows, cols] tensor map with a 128-byte-swizzled box of
 // box_cols x box_rows elements; reads past the edges return zeros.
 hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, size_t elem,
-                      int64_t cols, int64_t rows, uint32_t box_cols, uint32_t box_rows) {
+                      int64_t cols, int64_t rows, uint32_t box_cols, uint32_t box_rows,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(HESS_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -72,7 +73,7 @@ hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, s
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(HESS_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld]",
@@ -197,7 +198,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         const auto& q = h->pending[b];
         hess_status st =
             f32 ? encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, h->d, q.n, 32,
-                            hk::kKBlockF32)
+                            hk::kKBlockF32, hk::kF32Swizzle)
                 : encode_2d(&p.maps[b], q.ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->d, q.n, 64,
                             hk::kKBlock);
         if (st != HESS_OK) return st;

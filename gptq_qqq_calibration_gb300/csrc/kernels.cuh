@@ -17,6 +17,14 @@ constexpr int kTileElems = kTile * kTile;
 constexpr int kKBlock = 64;
 // Tokens per k-block of the fp32-input SYRK kernel.
 constexpr int kKBlockF32 = 32;
+// Shared-memory layout of the fp32 operand boxes.  MN-major tf32 operands of
+// tcgen05.mma need the 128-byte swizzle with 32-byte granules (TMA
+// SWIZZLE_128B_ATOM_32B, descriptor mode 1), whose K groups are 4 rows of
+// 128 bytes (stride 512 bytes).  Measured on GB300: the 16-byte-granule
+// swizzle gives zeros, and a 1,024-byte K-group stride gives wrong sums.
+constexpr CUtensorMapSwizzle kF32Swizzle = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+constexpr uint32_t kF32DescLayout = 1u;
+constexpr uint32_t kF32Sbo = 512u;
 // Batches one fused flush can hold; their tensor maps travel in the kernel
 // parameter block (up to 32 KB on sm_70 and later).
 constexpr int kMaxBatches = 192;

@@ -128,13 +128,16 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint6
 // For an MN-major operand: `lbo` is the byte distance between consecutive
 // 128-byte slices along M/N, `sbo` the distance between consecutive groups
 // of 8 rows along K.  Swizzle atoms must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// `layout` is the descriptor's swizzle mode: 2 = 128-byte swizzle (16-byte
+// granules), 1 = 128-byte swizzle with 32-byte granules.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                                    uint32_t layout = 2u) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;  // descriptor version for tcgen05
-    d |= 2ull << 61;  // 128-byte swizzle
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
 }
 

@@ -11,7 +11,8 @@
 //
 // How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
 //   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
-//     128-byte swizzle) into a 3-deep landing ring; the whole of warp 0 then
+//     128-byte swizzle with 32-byte granules, the layout MN-major tf32
+//     operands need) into a 3-deep landing ring; the whole of warp 0 then
 //     converts each landed stage into hi / lo planes of a 2-deep MMA ring,
 //     at the same byte offsets (so the swizzle carries over), and refills
 //     the landing slot at once;
@@ -237,10 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
 #pragma unroll
                         for (int j = 0; j < kKB / 8; ++j) {
                             const uint32_t off = j * 1024u;
-                            const uint64_t ahi = smem_desc_sw128(sA + off, kBoxBytes, 1024u);
-                            const uint64_t alo = smem_desc_sw128(sA + kOpBytes + off, kBoxBytes, 1024u);
-                            const uint64_t bhi = smem_desc_sw128(sB + off, kBoxBytes, 1024u);
-                            const uint64_t blo = smem_desc_sw128(sB + kOpBytes + off, kBoxBytes, 1024u);
+                            const uint64_t ahi = smem_desc_sw128(sA + off, kBoxBytes, kF32Sbo, kF32DescLayout);
+                            const uint64_t alo =
+                                smem_desc_sw128(sA + kOpBytes + off, kBoxBytes, kF32Sbo, kF32DescLayout);
+                            const uint64_t bhi = smem_desc_sw128(sB + off, kBoxBytes, kF32Sbo, kF32DescLayout);
+                            const uint64_t blo =
+                                smem_desc_sw128(sB + kOpBytes + off, kBoxBytes, kF32Sbo, kF32DescLayout);
                             const uint32_t acc = (kb > c0 || j > 0) ? 1u : 0u;
                             umma_tf32(d0, ahi, bhi, kIdesc, acc);
                             umma_tf32(d1, ahi, blo, kIdesc, acc);
