@@ -131,7 +131,8 @@ def run_ours(args):
     if args.batches:
         wl = wl.scaled(n_batches=args.batches)
     d = wl.d
-    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    in_dtype = torch.float32 if args.dtype == "f32" else torch.bfloat16
+    xs = [wl.batch(b, device="cuda", dtype=in_dtype) for b in range(len(wl.token_counts))]
     n_tok = wl.n_tokens
     flops = algo_flops(n_tok, d)
     h = Hessian(d)
@@ -172,7 +173,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
         "tokens_per_s": round(ws * n_tok / (ms * 1e-3), 1),
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
         "data": "synthetic (seeded torch.randn, per-channel std log-uniform [0.1, 10], rounded to bf16)",
         "config": {"workload": wl.name, "d": d, "batches": len(xs), "tokens": n_tok,
                    "token_counts": "uniform integers [1, 2000], numpy default_rng(3)",
@@ -181,7 +182,7 @@ def run_ours(args):
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(syrk_tflops, 2), "peak": bf16_sust,
                      "unit": "TFLOP/s", "frac": round(syrk_tflops / bf16_sust, 4), "traffic": None,
-                     "kernel": "syrk_bf16_kernel",
+                     "kernel": "syrk_%s_kernel" % args.dtype,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16, dense)",
                      "launches_timed": kern["launches"]},
         "e2e": e2e,
@@ -443,6 +444,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="d4096_ragged360_loguniform")
     ap.add_argument("--batches", type=int, default=0, help="use only the first K batches")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32"], help="input element type")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

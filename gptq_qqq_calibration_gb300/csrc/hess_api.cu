@@ -208,9 +208,9 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     p.total_kb = p.kb_start[nb];
     p.n_tiles = h->n_tiles;
     p.tiles_per_dim = h->T;
-    // fp32 input runs three MMAs per 8 tokens (hi*hi plus two cross terms), so
-    // its chains are 4x shorter in tokens for the same rounding bias.
-    p.chunk_kb = f32 ? std::max(1, h->chunk_tokens / 4 / hk::kKBlockF32)
+    // fp32 input has a 10x tighter bound and 2x more MMA steps per token, so
+    // its chains are 8x shorter in tokens.
+    p.chunk_kb = f32 ? std::max(1, h->chunk_tokens / 8 / hk::kKBlockF32)
                      : std::max(1, h->chunk_tokens / hk::kKBlock);
     p.d = static_cast<int32_t>(h->d);
     p.acc = h->acc;

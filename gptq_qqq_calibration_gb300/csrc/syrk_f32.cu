@@ -5,9 +5,9 @@
 // do?").  Here the same sums run on the tensor cores with a split that keeps
 // fp32 accuracy: every value is written x = hi + lo, hi = x rounded to
 // nearest tf32 (11 significant bits) and lo = x - hi (exact), and
-//     x_i x_j ~= hi_i hi_j + (hi_i lo_j + lo_i hi_j)
-// which drops only lo_i lo_j (relative <= 2^-22, zero mean because the
-// rounding is to nearest) and the tf32 truncation of lo (relative 2^-22).
+//     x_i x_j = hi_i hi_j + (hi_i lo_j + lo_i hi_j + lo_i lo_j)
+// where only the tf32 rounding of lo (relative 2^-22 of x, zero mean because
+// hi is rounded to nearest) is lost.
 //
 // How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
 //   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
@@ -17,12 +17,12 @@
 //     at the same byte offsets (so the swizzle carries over), and refills
 //     the landing slot at once;
 //   * warp 1 issues tcgen05.mma kind::tf32 (M=N=128, K=8): hi*hi into bank 0
-//     and the two cross terms into bank 1, so the small cross terms never
-//     ride on the large running sum;
+//     and the three small terms into bank 1, so they never ride on the
+//     large running sum;
 //   * warps 2-9 run the shared compensated epilogue (bank 0 + bank 1 folded
 //     into registers by TwoSum, fp64 add at the end of a unit).
-// Tensor-core accumulation rounds toward zero, so chunks are short (64
-// tokens by default: 8 hi*hi steps).  Every wait is bounded.
+// Tensor-core accumulation rounds toward zero, so chunks are short (32
+// tokens by default: 4 hi*hi steps).  Every wait is bounded.
 #include "syrk_common.cuh"
 
 namespace hk {
@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
                             umma_tf32(d0, ahi, bhi, kIdesc, acc);
                             umma_tf32(d1, ahi, blo, kIdesc, acc);
                             umma_tf32(d1, alo, bhi, kIdesc, 1u);
+                            umma_tf32(d1, alo, blo, kIdesc, 1u);
                         }
                         tc_commit(cvt_empty(cs));
                         ++consumed;

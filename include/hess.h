@@ -79,7 +79,7 @@ typedef enum {
                                      steps between two chains (64..65536, multiple of 64,
                                      default 256).  Tensor-core accumulation rounds toward
                                      zero, so longer chunks bias H low.  fp32 batches use
-                                     chunks of a quarter of this (at least 32 tokens). */
+                                     chunks of an eighth of this (at least 32 tokens). */
     HESS_OPT_WAIT_TIMEOUT_NS = 4, /* limit of every device-side wait, ns (default 2e9; 0 makes
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */
