@@ -81,17 +81,22 @@ hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, s
     return HESS_OK;
 }
 
-// Per-device one-time kernel set-up (dynamic shared-memory limits).
-hess_status prepare_device(int dev) {
+// Per-device one-time kernel set-up (dynamic shared-memory limits, how many
+// SM pairs the pair kernel can keep resident).
+hess_status prepare_device(int dev, int* max_pairs) {
     static std::mutex mu;
     static bool done[128] = {};
+    static int pairs[128] = {};
     std::lock_guard<std::mutex> lk(mu);
     if (dev < 0 || dev >= 128) return fail(HESS_ERR_UNSUPPORTED, "device index %d", dev);
-    if (done[dev]) return HESS_OK;
-    CUDA_TRY(hk::syrk_bf16_prepare());
-    CUDA_TRY(hk::syrk_f32_prepare());
-    CUDA_TRY(hk::local_prepare());
-    done[dev] = true;
+    if (!done[dev]) {
+        CUDA_TRY(hk::syrk_bf16_prepare());
+        CUDA_TRY(hk::syrk_bf16_2sm_prepare(&pairs[dev]));
+        CUDA_TRY(hk::syrk_f32_prepare());
+        CUDA_TRY(hk::local_prepare());
+        done[dev] = true;
+    }
+    if (max_pairs) *max_pairs = pairs[dev];
     return HESS_OK;
 }
 
@@ -132,6 +137,8 @@ struct hess_ctx {
     unsigned long long timeout_ns = 2000000000ull;
     int split_k = 0;
     int grid = 0;
+    int pair_kernel = 1;  // bf16: 1 = pairs of SMs (256 x 128 tiles), 0 = one SM per tile
+    int max_pairs = 0;
     hk::SyrkParams* params = nullptr;  // host staging of the launch parameters
 };
 
@@ -216,12 +223,25 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     p.acc = h->acc;
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
-    const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
-    p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
-                               : choose_slabs(h->n_tiles, p.total_kb, grid_max);
-    p.n_units = p.n_tiles * p.n_slabs;
-    const int grid = std::min(grid_max, p.n_units);
-    cudaError_t e = f32 ? hk::launch_syrk_f32(p, grid, stream) : hk::launch_syrk_bf16(p, grid, stream);
+    const bool pairs = !f32 && h->pair_kernel && h->max_pairs > 0;
+    int grid = 0;
+    cudaError_t e;
+    if (pairs) {
+        p.n_tiles = hk::pair_tile_count(h->T);
+        const int pairs_max = h->grid > 0 ? std::max(1, std::min(h->grid / 2, h->max_pairs)) : h->max_pairs;
+        p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
+                                   : choose_slabs(p.n_tiles, p.total_kb, pairs_max);
+        p.n_units = p.n_tiles * p.n_slabs;
+        grid = 2 * std::min(pairs_max, p.n_units);
+        e = hk::launch_syrk_bf16_2sm(p, grid, stream);
+    } else {
+        const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
+        p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
+                                   : choose_slabs(h->n_tiles, p.total_kb, grid_max);
+        p.n_units = p.n_tiles * p.n_slabs;
+        grid = std::min(grid_max, p.n_units);
+        e = f32 ? hk::launch_syrk_f32(p, grid, stream) : hk::launch_syrk_bf16(p, grid, stream);
+    }
     h->pending.clear();
     h->pending_tokens = 0;
     h->pending_dtype = -1;
@@ -229,7 +249,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     if (std::getenv("HESS_TRACE"))
         std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d grid=%d %s\n",
                      static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, grid,
-                     f32 ? "f32" : "bf16");
+                     f32 ? "f32" : (pairs ? "bf16-pairs" : "bf16"));
     return HESS_OK;
 }
 
@@ -254,7 +274,8 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     if (injected_alloc_failure()) return fail(HESS_ERR_OOM, "injected allocation failure (HESS_FAULT=alloc)");
     int dev = 0;
     CUDA_TRY(cudaGetDevice(&dev));
-    hess_status st = prepare_device(dev);
+    int max_pairs = 0;
+    hess_status st = prepare_device(dev, &max_pairs);
     if (st != HESS_OK) return st;
     hess_ctx* h = new (std::nothrow) hess_ctx();
     if (!h) return fail(HESS_ERR_OOM, "host allocation failed");
@@ -264,6 +285,7 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
         return fail(HESS_ERR_OOM, "host allocation failed");
     }
     h->device = dev;
+    h->max_pairs = max_pairs;
     h->d = d;
     h->T = static_cast<int>(ceil_div(d, hk::kTile));
     h->n_tiles = h->T * (h->T + 1) / 2;
@@ -435,6 +457,10 @@ HESS_EXPORT hess_status hess_set_option(hess_t h, int32_t option, int64_t value)
             if (value < 0 || value > 65535) return fail(HESS_ERR_INVALID, "grid must be in [0, 65535]");
             h->grid = static_cast<int>(value);
             return HESS_OK;
+        case HESS_OPT_PAIR_KERNEL:
+            if (value != 0 && value != 1) return fail(HESS_ERR_INVALID, "pair_kernel must be 0 or 1");
+            h->pair_kernel = static_cast<int>(value);
+            return HESS_OK;
         default:
             return fail(HESS_ERR_INVALID, "unknown option %d", option);
     }
@@ -472,7 +498,7 @@ HESS_EXPORT hess_status local_hess_create(int64_t d, int32_t block, local_hess_t
     if (injected_alloc_failure()) return fail(HESS_ERR_OOM, "injected allocation failure (HESS_FAULT=alloc)");
     int dev = 0;
     CUDA_TRY(cudaGetDevice(&dev));
-    hess_status st = prepare_device(dev);
+    hess_status st = prepare_device(dev, nullptr);
     if (st != HESS_OK) return st;
     local_hess_ctx* h = new (std::nothrow) local_hess_ctx();
     if (!h) return fail(HESS_ERR_OOM, "host allocation failed");

@@ -61,6 +61,17 @@ size_t syrk_bf16_smem_bytes();
 cudaError_t syrk_bf16_prepare();  // sets the dynamic shared-memory limit (per device)
 cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s);
 
+// Pair-of-SMs bf16 kernel (256 x 128 tiles): n_tiles counts pair tiles,
+// sum over I2 < ceil(T/2) of (T - 2*I2); the grid is 2 CTAs per pair.
+size_t syrk_bf16_2sm_smem_bytes();
+cudaError_t syrk_bf16_2sm_prepare(int* max_pairs);
+cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s);
+__host__ __device__ inline int pair_tile_count(int T) {
+    int n = 0;
+    for (int i = 0; 2 * i < T; ++i) n += T - 2 * i;
+    return n;
+}
+
 size_t syrk_f32_smem_bytes();
 cudaError_t syrk_f32_prepare();
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);

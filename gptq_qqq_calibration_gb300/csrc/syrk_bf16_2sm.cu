@@ -1,0 +1,288 @@
+// Symmetric rank-k update S += X^T X for bf16 activations, run by pairs of
+// SMs (tcgen05 cta_group::2) on 256 x 128 tiles.
+//
+// Same sums as syrk_bf16.cu (GPTQModel PR #2979 Summary; NVIDIA
+// Model-Optimizer PR #3002, "What does this PR do?"), laid out for the
+// per-SM operand ingress that bounds the single-SM kernel (about 58 bytes per
+// clock per SM on GB300, measured): a pair computes a 256-row x 128-column
+// tile, each SM receiving its 128 rows of A and 64 of the 128 columns of B,
+// i.e. 24 KB per 64 tokens instead of 32 KB for the same tensor work.
+//
+// Tiles: rows in blocks of 256 (I2), columns in blocks of 128 (J), J >= 2*I2
+// so that the upper triangle is covered.  CTA r of the pair owns rows
+// 256*I2 + 128*r .. +127 of the tile, i.e. 128x128 accumulator tile
+// (2*I2 + r, J); blocks strictly below the diagonal are computed (the MMA
+// spans 256 rows) but not stored.
+//
+// Roles (both CTAs run all of them, except where noted):
+//   * warp 0: TMA producer for this CTA's A (2 boxes) and B (1 box), into an
+//     8-deep ring, signalling this CTA's own barrier;
+//   * warp 1 of the even CTA: issues tcgen05.mma.cta_group::2 (M=256, N=128,
+//     K=16), alternating 16-token steps between two accumulator banks, and
+//     multicasts every commit to both CTAs;
+//   * warp 1 of the odd CTA: forwards "stage landed" to the even CTA with a
+//     cluster-scope arrive, so every CTA can drain its own copies;
+//   * warps 2-9: the shared compensated epilogue on this CTA's 128 rows; they
+//     release accumulator buffers on the even CTA's barrier.
+// Every wait is bounded; both CTAs meet at a cluster barrier before tensor
+// memory is freed, so neither exits while the other still reads its memory.
+#include "syrk_common.cuh"
+
+namespace hk {
+namespace {
+
+using syrk::kDrainLimitNs;
+using syrk::kEpiWarps;
+
+constexpr int kStages = 8;
+constexpr uint32_t kBoxBytes = 64 * 128;            // 64 tokens x 64 bf16
+constexpr uint32_t kABytes = 2 * kBoxBytes;         // this CTA's 128 rows
+constexpr uint32_t kBBytes = kBoxBytes;             // this CTA's 64 columns
+constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 24 KB
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 256, 128);
+constexpr int kNumBarriers = 3 * kStages + 5;
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBarriers + 16;
+
+struct PairUnit {
+    int I2, J, k0, k1;
+};
+
+__device__ __forceinline__ bool pair_unit_at(const SyrkParams& p, int u, PairUnit& un) {
+    const int slab = u / p.n_tiles;
+    const int t = u - slab * p.n_tiles;
+    const int T = p.tiles_per_dim;
+    int i = 0, rem = t;
+    while (rem >= T - 2 * i) {
+        rem -= T - 2 * i;
+        ++i;
+    }
+    un.I2 = i;
+    un.J = 2 * i + rem;
+    un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
+    un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
+    return un.k1 > un.k0;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    syrk_bf16_2sm_kernel(const __grid_constant__ SyrkParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + kStages * kStageBytes;
+    uint32_t* const tmem_slot =
+        reinterpret_cast<uint32_t*>(gbase + kStages * kStageBytes + 8 * kNumBarriers);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto ready_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * kStages + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    const int n_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(ready_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 2 * kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const unsigned long long limit = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_par = 0;
+            for (int u = pair; ok && u < p.n_units; u += n_pairs) {
+                PairUnit un;
+                if (!pair_unit_at(p, u, un)) continue;
+                const int xa = un.I2 * 256 + static_cast<int>(rank) * 128;
+                const int xb = un.J * kTile + static_cast<int>(rank) * 64;
+                int b = 0;
+                while (p.kb_start[b + 1] <= un.k0) ++b;
+                for (int kb = un.k0; kb < un.k1; ++kb) {
+                    while (p.kb_start[b + 1] <= kb) ++b;
+                    const int tok = (kb - p.kb_start[b]) * kKBlock;
+                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const CUtensorMap* m = &p.maps[b];
+                    const uint32_t sA = base + stage * kStageBytes;
+                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    tma_load_2d(sA, m, full_bar(stage), xa, tok);
+                    tma_load_2d(sA + kBoxBytes, m, full_bar(stage), xa + 64, tok);
+                    tma_load_2d(sA + kABytes, m, full_bar(stage), xb, tok);
+                    issued |= 1u << stage;
+                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
+            for (int s = 0; s < kStages; ++s)
+                if ((issued >> s) & 1u)
+                    if (!mbar_wait(full_bar(s), (issued_par >> s) & 1u, kDrainLimitNs))
+                        atomicOr(p.status, kStatusTimeoutDrain);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // -------------------------------------------- MMA issuer (even CTA)
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            int ab = 0;
+            uint32_t aphase = 0;
+            for (int u = pair; ok && u < p.n_units; u += n_pairs) {
+                PairUnit un;
+                if (!pair_unit_at(p, u, un)) continue;
+                for (int c0 = un.k0; c0 < un.k1; c0 += p.chunk_kb) {
+                    const int c1 = min(c0 + p.chunk_kb, un.k1);
+                    if (!mbar_wait_cluster(acce_bar(ab), aphase ^ 1u, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dt = tmem + static_cast<uint32_t>(ab) * 256u;
+                    for (int kb = c0; kb < c1; ++kb) {
+                        if (!mbar_wait(full_bar(stage), phase, limit) ||
+                            !mbar_wait_cluster(ready_bar(stage), phase, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sA = base + stage * kStageBytes;
+                        const uint32_t sB = sA + kABytes;
+#pragma unroll
+                        for (int j = 0; j < kKBlock / 16; ++j) {
+                            const uint64_t ad = smem_desc_sw128(sA + j * 2048u, kBoxBytes, 1024u);
+                            // B is one 64-column slice per CTA: no second slice to
+                            // stride to (a zero stride keeps any read inside it)
+                            const uint64_t bd = smem_desc_sw128(sB + j * 2048u, 0u, 1024u);
+                            umma_f16_pair(dt + (j & 1) * 128u, ad, bd, kIdesc,
+                                          (kb > c0 || j > 1) ? 1u : 0u);
+                        }
+                        tc_commit_pair_mc(empty_bar(stage), 0x3);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_mc(accf_bar(ab), 0x3);
+                    if (++ab == 2) {
+                        ab = 0;
+                        aphase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutMma);
+            // Wait for every MMA issued before the pair's memories are released.
+            tc_commit_pair_mc(drain_bar, 0x1);
+            if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
+        } else if (lane == 0) {
+            // -------------------------------------------- forwarder (odd CTA)
+            bool ok = true;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int u = pair; ok && u < p.n_units; u += n_pairs) {
+                PairUnit un;
+                if (!pair_unit_at(p, u, un)) continue;
+                for (int kb = un.k0; kb < un.k1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (8 warps)
+        const int T = p.tiles_per_dim;
+        const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+        syrk::epilogue_t(
+            p, tmem, warp, lane, 2, accf_bar(0), pair, n_pairs,
+            [&](int u, int& k0, int& k1, int& out_tile) {
+                PairUnit un;
+                if (!pair_unit_at(p, u, un)) return false;
+                k0 = un.k0;
+                k1 = un.k1;
+                const int rb = 2 * un.I2 + static_cast<int>(rank);
+                out_tile = (rb < T && rb <= un.J) ? tile_index(rb, un.J, T) : -1;
+                return true;
+            },
+            [&](uint32_t bar, uint32_t parity) { return mbar_wait_cluster(bar, parity, limit); },
+            [&](int b) { mbar_arrive_cluster(acce_leader0 + 8u * b); });
+    }
+
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t syrk_bf16_2sm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
+    cudaError_t e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, syrk_bf16_2sm_kernel, &cfg);
+    if (e != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        clusters = sms / 2;
+    }
+    *max_pairs = clusters;
+    return cudaSuccess;
+}
+
+cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s) {
+    syrk_bf16_2sm_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace hk

@@ -39,10 +39,15 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 // sits in buffer (chunk counter & 1).  Each warp reads its lane quarter
 // (warp % 4) and one half of the columns, adds the two banks, and folds the
 // sum into a (hi, lo) pair with an exact TwoSum on packed fp32 pairs.  At the
-// end of a unit, hi + lo is added in fp64 to the accumulator.
-__device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int warp, int lane,
-                                         int first_warp, uint32_t accf_bar0, uint32_t acce_bar0,
-                                         unsigned long long limit) {
+// end of a unit, hi + lo is added in fp64 to accumulator tile `out_tile`
+// (skipped when it is negative).
+//   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
+//   wait_full(bar, parity) waits for a filled accumulator buffer;
+//   arrive_empty(b) releases buffer b to the MMA issuer.
+template <class UnitFn, class WaitFn, class ArriveFn>
+__device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, int warp, int lane,
+                                           int first_warp, uint32_t accf_bar0, int u0, int ustride,
+                                           UnitFn unit_fn, WaitFn wait_full, ArriveFn arrive_empty) {
     const int q = warp & 3;
     const int half = (warp - first_warp) >> 2;
     const int row = q * 32 + lane;
@@ -52,14 +57,12 @@ __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int
     bool ok = true;
     int ab = 0;
     uint32_t aphase = 0;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        Unit un;
-        if (!unit_at(p, u, un)) continue;
-        const int nch = (un.k1 - un.k0 + p.chunk_kb - 1) / p.chunk_kb;
-        double* const out = p.acc + static_cast<size_t>(un.t) * kTileElems +
-                            static_cast<size_t>(col0) * kTile + row;
+    for (int u = u0; ok && u < p.n_units; u += ustride) {
+        int k0, k1, out_tile;
+        if (!unit_fn(u, k0, k1, out_tile)) continue;
+        const int nch = (k1 - k0 + p.chunk_kb - 1) / p.chunk_kb;
         for (int c = 0; c < nch; ++c) {
-            if (!mbar_wait(accf_bar0 + 8u * ab, aphase, limit)) {
+            if (!wait_full(accf_bar0 + 8u * ab, aphase)) {
                 ok = false;
                 break;
             }
@@ -86,13 +89,16 @@ __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar0 + 8u * ab);
+            if (lane == 0) arrive_empty(ab);
             if (++ab == 2) {
                 ab = 0;
                 aphase ^= 1u;
             }
         }
         if (!ok) break;
+        if (out_tile < 0) continue;
+        double* const out = p.acc + static_cast<size_t>(out_tile) * kTileElems +
+                            static_cast<size_t>(col0) * kTile + row;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             float h0, h1, l0, l1;
@@ -103,6 +109,24 @@ __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int
         }
     }
     if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);
+}
+
+// The single-CTA form: units in blockIdx.x + k * gridDim.x order, local barriers.
+__device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int warp, int lane,
+                                         int first_warp, uint32_t accf_bar0, uint32_t acce_bar0,
+                                         unsigned long long limit) {
+    epilogue_t(
+        p, tmem, warp, lane, first_warp, accf_bar0, blockIdx.x, gridDim.x,
+        [&](int u, int& k0, int& k1, int& out_tile) {
+            Unit un;
+            if (!unit_at(p, u, un)) return false;
+            k0 = un.k0;
+            k1 = un.k1;
+            out_tile = un.t;
+            return true;
+        },
+        [&](uint32_t bar, uint32_t parity) { return mbar_wait(bar, parity, limit); },
+        [&](int b) { mbar_arrive(acce_bar0 + 8u * b); });
 }
 
 }  // namespace syrk

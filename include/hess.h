@@ -83,7 +83,9 @@ typedef enum {
     HESS_OPT_WAIT_TIMEOUT_NS = 4, /* limit of every device-side wait, ns (default 2e9; 0 makes
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */
-    HESS_OPT_GRID = 6             /* persistent CTAs per flush; 0 = one per SM (default) */
+    HESS_OPT_GRID = 6,            /* persistent CTAs per flush; 0 = one per SM (default) */
+    HESS_OPT_PAIR_KERNEL = 7      /* bf16: 1 = tiles of 256x128 on pairs of SMs (default),
+                                     0 = tiles of 128x128, one SM each */
 } hess_option;
 
 /* ------------------------------------------------------------------------ */

@@ -40,6 +40,7 @@ def _run(d, counts, seed, damp=0.01, profile="normal", dtype=torch.bfloat16, **o
     return Hn, dv, Href, dref
 
 
+@pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("d,counts", [
     (256, [128, 128, 128, 128]),
     (136, [1, 63, 64, 65, 200]),
@@ -48,8 +49,8 @@ def _run(d, counts, seed, damp=0.01, profile="normal", dtype=torch.bfloat16, **o
     (384, [333, 0, 1, 130]),
     (640, [1000]),
 ])
-def test_bf16_matches_oracle(d, counts):
-    H, dv, Href, dref = _run(d, counts, seed=d)
+def test_bf16_matches_oracle(d, counts, pair):
+    H, dv, Href, dref = _run(d, counts, seed=d, pair_kernel=pair)
     assert rel_err(H, Href) <= TOL_BF16
     assert np.array_equal(H, H.T), "H_out must be bit-exactly symmetric"
     assert dv == pytest.approx(dref, rel=TOL_BF16)
@@ -57,8 +58,10 @@ def test_bf16_matches_oracle(d, counts):
 
 @pytest.mark.parametrize("opts", [
     dict(chunk_tokens=64), dict(chunk_tokens=128, split_k=3), dict(split_k=7),
-    dict(grid=5), dict(grid=1, chunk_tokens=64), dict(flush_tokens=1),
+    dict(grid=4), dict(grid=2, chunk_tokens=64), dict(flush_tokens=1),
     dict(max_pending=3, chunk_tokens=4096), dict(split_k=40),
+    dict(pair_kernel=0), dict(pair_kernel=0, split_k=3, grid=5),
+    dict(pair_kernel=0, grid=1, chunk_tokens=64), dict(pair_kernel=0, flush_tokens=1),
 ])
 def test_bf16_schedules(opts):
     H, dv, Href, dref = _run(512, [700, 1, 64, 129, 512, 33], seed=11, **opts)
