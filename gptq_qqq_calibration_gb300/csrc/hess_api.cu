@@ -137,7 +137,7 @@ struct hess_ctx {
     unsigned long long timeout_ns = 2000000000ull;
     int split_k = 0;
     int grid = 0;
-    int pair_kernel = 1;  // bf16: 1 = pairs of SMs (256 x 128 tiles), 0 = one SM per tile
+    int pair_kernel = 0;  // bf16: 1 = pairs of SMs (256 x 128 tiles), 0 = one SM per tile
     int max_pairs = 0;
     hk::SyrkParams* params = nullptr;  // host staging of the launch parameters
 };
@@ -228,7 +228,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     cudaError_t e;
     if (pairs) {
         p.n_tiles = hk::pair_tile_count(h->T);
-        const int pairs_max = h->grid > 0 ? std::max(1, std::min(h->grid / 2, h->max_pairs)) : h->max_pairs;
+        const int pairs_max = h->grid > 0 ? std::max(1, h->grid / 2) : h->max_pairs;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(p.n_tiles, p.total_kb, pairs_max);
         p.n_units = p.n_tiles * p.n_slabs;
@@ -247,9 +247,9 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     h->pending_dtype = -1;
     if (e != cudaSuccess) return fail(HESS_ERR_CUDA, "SYRK launch failed: %s", cudaGetErrorString(e));
     if (std::getenv("HESS_TRACE"))
-        std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d grid=%d %s\n",
+        std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d grid=%d %s (max pairs %d)\n",
                      static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, grid,
-                     f32 ? "f32" : (pairs ? "bf16-pairs" : "bf16"));
+                     f32 ? "f32" : (pairs ? "bf16-pairs" : "bf16"), h->max_pairs);
     return HESS_OK;
 }
 

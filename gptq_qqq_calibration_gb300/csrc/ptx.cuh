@@ -289,6 +289,25 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Arrive (relaxed, cluster scope): no ordering of this thread's earlier
+// memory operations, only the arrival itself.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (`bar` is a shared::cluster
+// address, e.g. the even CTA's barrier obtained with mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
 // try_wait with acquire at cluster scope (for barriers a peer CTA arrives on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -344,6 +363,14 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
         " [%0], %1;" ::"r"(bar),
         "h"(mask)
         : "memory");
+}
+
+// Fast2Sum on pairs: s + err == a + b exactly when |a| >= |b| (element-wise);
+// otherwise err is off by at most an ulp of s, like a plain rounded add.
+__device__ __forceinline__ uint64_t fast_two_sum2(uint64_t a, uint64_t b, uint64_t& err) {
+    const uint64_t s = add2(a, b);
+    err = sub2(b, sub2(s, a));
+    return s;
 }
 
 // ------------------------------------------------------------ global memory

@@ -16,16 +16,19 @@
 //
 // Roles (both CTAs run all of them, except where noted):
 //   * warp 0: TMA producer for this CTA's A (2 boxes) and B (1 box), into an
-//     8-deep ring, signalling this CTA's own barrier;
+//     8-deep ring; the copies of both CTAs count their bytes on the even
+//     CTA's barrier (pair-mode TMA), which expects both;
 //   * warp 1 of the even CTA: issues tcgen05.mma.cta_group::2 (M=256, N=128,
 //     K=16), alternating 16-token steps between two accumulator banks, and
 //     multicasts every commit to both CTAs;
-//   * warp 1 of the odd CTA: forwards "stage landed" to the even CTA with a
-//     cluster-scope arrive, so every CTA can drain its own copies;
 //   * warps 2-9: the shared compensated epilogue on this CTA's 128 rows; they
-//     release accumulator buffers on the even CTA's barrier.
+//     release accumulator buffers on the even CTA's barrier (relaxed arrive:
+//     their tensor-memory loads have completed, and a release would wait for
+//     the unrelated fp64 reductions still in flight).
 // Every wait is bounded; both CTAs meet at a cluster barrier before tensor
 // memory is freed, so neither exits while the other still reads its memory.
+// After a timeout a CTA cannot watch its own copies land (they count on the
+// even CTA's barrier), so it pauses 2 ms before that barrier.
 #include "syrk_common.cuh"
 
 namespace hk {
@@ -42,7 +45,8 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 24 KB
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 256, 128);
-constexpr int kNumBarriers = 3 * kStages + 5;
+constexpr int kNumBarriers = 2 * kStages + 5;
+constexpr unsigned long long kAbortSettleNs = 2000000ull;
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBarriers + 16;
 
 struct PairUnit {
@@ -75,11 +79,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t* const tmem_slot =
         reinterpret_cast<uint32_t*>(gbase + kStages * kStageBytes + 8 * kNumBarriers);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto ready_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-    auto accf_bar = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
-    auto acce_bar = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * kStages + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    __shared__ int aborted;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -90,9 +94,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(ready_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
+        aborted = 0;
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 2 * kEpiWarps);
@@ -115,7 +119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             bool ok = true;
             int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_par = 0;
+            uint32_t phase = 0;
             for (int u = pair; ok && u < p.n_units; u += n_pairs) {
                 PairUnit un;
                 if (!pair_unit_at(p, u, un)) continue;
@@ -132,23 +136,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     const CUtensorMap* m = &p.maps[b];
                     const uint32_t sA = base + stage * kStageBytes;
-                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-                    tma_load_2d(sA, m, full_bar(stage), xa, tok);
-                    tma_load_2d(sA + kBoxBytes, m, full_bar(stage), xa + 64, tok);
-                    tma_load_2d(sA + kABytes, m, full_bar(stage), xb, tok);
-                    issued |= 1u << stage;
-                    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+                    tma_load_2d_pair(sA, m, fb, xa, tok);
+                    tma_load_2d_pair(sA + kBoxBytes, m, fb, xa + 64, tok);
+                    tma_load_2d_pair(sA + kABytes, m, fb, xb, tok);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
-            for (int s = 0; s < kStages; ++s)
-                if ((issued >> s) & 1u)
-                    if (!mbar_wait(full_bar(s), (issued_par >> s) & 1u, kDrainLimitNs))
-                        atomicOr(p.status, kStatusTimeoutDrain);
+            if (!ok) {
+                atomicOr(p.status, kStatusTimeoutLoad);
+                aborted = 1;
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
@@ -170,8 +172,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t dt = tmem + static_cast<uint32_t>(ab) * 256u;
                     for (int kb = c0; kb < c1; ++kb) {
-                        if (!mbar_wait(full_bar(stage), phase, limit) ||
-                            !mbar_wait_cluster(ready_bar(stage), phase, limit)) {
+                        if (!mbar_wait_cluster(full_bar(stage), phase, limit)) {
                             ok = false;
                             break;
                         }
@@ -201,31 +202,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) atomicOr(p.status, kStatusTimeoutMma);
+            if (!ok) {
+                atomicOr(p.status, kStatusTimeoutMma);
+                aborted = 1;
+            }
             // Wait for every MMA issued before the pair's memories are released.
             tc_commit_pair_mc(drain_bar, 0x1);
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
-        } else if (lane == 0) {
-            // -------------------------------------------- forwarder (odd CTA)
-            bool ok = true;
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int u = pair; ok && u < p.n_units; u += n_pairs) {
-                PairUnit un;
-                if (!pair_unit_at(p, u, un)) continue;
-                for (int kb = un.k0; kb < un.k1; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
         }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
@@ -243,7 +226,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 return true;
             },
             [&](uint32_t bar, uint32_t parity) { return mbar_wait_cluster(bar, parity, limit); },
-            [&](int b) { mbar_arrive_cluster(acce_leader0 + 8u * b); });
+            [&](int b) { mbar_arrive_cluster_relaxed(acce_leader0 + 8u * b); });
+        if (p.status != nullptr && lane == 0 && *reinterpret_cast<volatile uint32_t*>(p.status) != 0)
+            aborted = 1;
+    }
+
+    // After a timeout, give copies that count on the peer's barrier time to land.
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(&aborted) != 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kAbortSettleNs) __nanosleep(1000);
     }
 
     tc_fence_before();

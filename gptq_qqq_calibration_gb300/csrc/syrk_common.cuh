@@ -31,14 +31,15 @@ __device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
     return un.k1 > un.k0;
 }
 
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;                   // 2 per tensor-memory lane quarter
+constexpr int kEpiCols = 4 * 128 / kEpiWarps;  // accumulator columns per warp
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
-// Epilogue of one CTA (8 warps, warps first_warp .. first_warp + 7).
+// Epilogue of one CTA (kEpiWarps warps starting at first_warp).
 // Tensor memory holds 2 buffers x 2 banks x 128 columns; chunk c of a unit
 // sits in buffer (chunk counter & 1).  Each warp reads its lane quarter
-// (warp % 4) and one half of the columns, adds the two banks, and folds the
-// sum into a (hi, lo) pair with an exact TwoSum on packed fp32 pairs.  At the
+// (warp % 4) and kEpiCols of the 128 columns, adds the two banks, and folds the
+// sum into a (hi, lo) pair with Fast2Sum on packed fp32 pairs.  At the
 // end of a unit, hi + lo is added in fp64 to accumulator tile `out_tile`
 // (skipped when it is negative).
 //   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
@@ -49,11 +50,11 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
                                            int first_warp, uint32_t accf_bar0, int u0, int ustride,
                                            UnitFn unit_fn, WaitFn wait_full, ArriveFn arrive_empty) {
     const int q = warp & 3;
-    const int half = (warp - first_warp) >> 2;
+    const int part = (warp - first_warp) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(half) * 64u;
-    uint64_t hi[32], lo[32];  // 64 columns of this thread's row, as pairs
+    const uint32_t col0 = static_cast<uint32_t>(part) * kEpiCols;
+    uint64_t hi[kEpiCols / 2], lo[kEpiCols / 2];  // this thread's columns, as pairs
     bool ok = true;
     int ab = 0;
     uint32_t aphase = 0;
@@ -69,7 +70,7 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
             tc_fence_after();
             const uint32_t tb = tmem + lane_off + static_cast<uint32_t>(ab) * 256u + col0;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
+            for (int it = 0; it < kEpiCols / 8; ++it) {
                 uint32_t b0[8], b1[8];
                 tmem_ld8x2_sync(tb + it * 8, tb + 128 + it * 8, b0, b1);
 #pragma unroll
@@ -81,8 +82,11 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
                         hi[i] = v;
                         lo[i] = 0ull;
                     } else {
+                        // The running sum dominates the chunk for the large
+                        // (diagonal-like) entries that set the error, where
+                        // Fast2Sum is exact; elsewhere it errs like one add.
                         uint64_t e;
-                        hi[i] = two_sum2(hi[i], v, e);
+                        hi[i] = fast_two_sum2(hi[i], v, e);
                         lo[i] = add2(lo[i], e);
                     }
                 }
@@ -100,7 +104,7 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         double* const out = p.acc + static_cast<size_t>(out_tile) * kTileElems +
                             static_cast<size_t>(col0) * kTile + row;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kEpiCols / 2; ++i) {
             float h0, h1, l0, l1;
             unpack2(hi[i], h0, h1);
             unpack2(lo[i], l0, l1);

@@ -84,8 +84,9 @@ typedef enum {
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */
     HESS_OPT_GRID = 6,            /* persistent CTAs per flush; 0 = one per SM (default) */
-    HESS_OPT_PAIR_KERNEL = 7      /* bf16: 1 = tiles of 256x128 on pairs of SMs (default),
-                                     0 = tiles of 128x128, one SM each */
+    HESS_OPT_PAIR_KERNEL = 7      /* bf16: 0 = tiles of 128x128, one SM each (default),
+                                     1 = tiles of 256x128 on pairs of SMs (fewer operand
+                                     bytes per SM; faster with long chunks) */
 } hess_option;
 
 /* ------------------------------------------------------------------------ */
