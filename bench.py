@@ -326,6 +326,32 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "peak_source": "bf16_tflops (burst) x 1/2 (nominal tf32:bf16 ratio)"}}
     h.close()
     del xs
+    # imatrix column sums of squares over the same local workload's batches
+    wl = WORKLOADS["local_d4096_8x32768"]
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    from gptq_qqq_calibration_gb300 import IMatrix
+    im = IMatrix(wl.d)
+    for X in xs:
+        im.add_batch(X)
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(3):
+        for X in xs:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            im.add_batch(X)
+            b.record()
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    per = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e-3
+    nbytes = xs[0].numel() * 2
+    out["imatrix"] = {
+        "workload": "column sums of squares, 32768 x 4096 bf16 per update", "us_per_update": round(per * 1e6, 2),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / per / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(nbytes / per / 1e9 / hbm, 4), "kernel": "colsumsq_kernel"}}
+    im.close()
+    del xs
     # local_hessian: 8 updates of 32768 tokens at d = 4096
     wl = WORKLOADS["local_d4096_8x32768"]
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]

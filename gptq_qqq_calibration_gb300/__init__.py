@@ -8,4 +8,4 @@ C ABI in ``include/hess.h``; this package only marshals arguments.
 """
 
 from .hessian import *  # noqa: F401,F403
-from .hessian import Hessian, LocalHessian  # noqa: F401
+from .hessian import Hessian, IMatrix, LocalHessian  # noqa: F401

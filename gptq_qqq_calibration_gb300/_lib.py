@@ -35,6 +35,14 @@ PROTOTYPES = {
     "hess_reset": (_i32, [_vp, _vp]),
     "hess_set_option": (_i32, [_vp, _i32, _i64]),
     "hess_destroy": (_i32, [_vp]),
+    "hess_merge": (_i32, [_vp, _vp, _vp]),
+    "hess_clone": (_i32, [_vp, ctypes.POINTER(_vp), _vp]),
+    "imatrix_create": (_i32, [_i64, ctypes.POINTER(_vp)]),
+    "imatrix_add": (_i32, [_vp, _vp, _i64, _i32, _vp]),
+    "imatrix_read": (_i32, [_vp, _vp, _vp]),
+    "imatrix_token_count": (_i64, [_vp]),
+    "imatrix_reset": (_i32, [_vp, _vp]),
+    "imatrix_destroy": (_i32, [_vp]),
     "local_hess_create": (_i32, [_i64, _i32, ctypes.POINTER(_vp)]),
     "local_hess_add": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "local_hess_read": (_i32, [_vp, _vp, _vp]),

@@ -486,6 +486,162 @@ HESS_EXPORT hess_status hess_destroy(hess_t h) {
     return HESS_OK;
 }
 
+// ------------------------------------------------- merge and clone (f2, f4)
+
+HESS_EXPORT hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream) {
+    if (!dst || !src) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (dst == src) return fail(HESS_ERR_INVALID, "cannot merge a handle into itself");
+    if (dst->d != src->d) return fail(HESS_ERR_INVALID, "widths differ (%lld vs %lld)",
+                                      (long long)dst->d, (long long)src->d);
+    if (dst->device != src->device)
+        return fail(HESS_ERR_UNSUPPORTED, "handles live on different devices");
+    // Lock in address order so that two merges in opposite directions cannot deadlock.
+    std::mutex& m1 = dst < src ? dst->mu : src->mu;
+    std::mutex& m2 = dst < src ? src->mu : dst->mu;
+    std::lock_guard<std::mutex> l1(m1);
+    std::lock_guard<std::mutex> l2(m2);
+    hess_status st = check_device(dst->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = flush_locked(src, s)) != HESS_OK) return st;
+    if ((st = flush_locked(dst, s)) != HESS_OK) return st;
+    const size_t n = static_cast<size_t>(dst->n_tiles) * hk::kTileElems;
+    CUDA_TRY(hk::launch_add_f64(dst->acc, src->acc, n, dst->sm_count, s));
+    dst->N += src->N;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream) {
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (!src) return fail(HESS_ERR_INVALID, "handle is NULL");
+    hess_t h = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(src->mu);
+        hess_status st = check_device(src->device);
+        if (st != HESS_OK) return st;
+        st = flush_locked(src, static_cast<cudaStream_t>(stream));
+        if (st != HESS_OK) return st;
+    }
+    hess_status st = hess_create(src->d, &h);
+    if (st != HESS_OK) return st;
+    std::lock_guard<std::mutex> lk(src->mu);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = static_cast<size_t>(src->n_tiles) * hk::kTileElems * sizeof(double);
+    cudaError_t e = cudaMemcpyAsync(h->acc, src->acc, bytes, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) {
+        hess_destroy(h);
+        return fail(HESS_ERR_CUDA, "clone copy failed: %s", cudaGetErrorString(e));
+    }
+    h->N = src->N;
+    h->flush_tokens = src->flush_tokens;
+    h->max_pending = src->max_pending;
+    h->chunk_tokens = src->chunk_tokens;
+    h->timeout_ns = src->timeout_ns;
+    h->split_k = src->split_k;
+    h->grid = src->grid;
+    h->pair_kernel = src->pair_kernel;
+    *out = h;
+    return HESS_OK;
+}
+
+// ----------------------------------------------------------- imatrix (f3)
+
+struct imatrix_ctx {
+    std::mutex mu;
+    int device = 0;
+    int64_t d = 0;
+    int sm_count = 0;
+    double* acc = nullptr;
+    int64_t N = 0;
+};
+
+HESS_EXPORT hess_status imatrix_create(int64_t d, imatrix_t* out) {
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d <= 0) return fail(HESS_ERR_INVALID, "d must be positive");
+    if (d % 8 != 0) return fail(HESS_ERR_UNSUPPORTED, "d = %lld is not a multiple of 8", (long long)d);
+    if (d > (int64_t(1) << 24)) return fail(HESS_ERR_UNSUPPORTED, "d too large");
+    if (injected_alloc_failure()) return fail(HESS_ERR_OOM, "injected allocation failure (HESS_FAULT=alloc)");
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    imatrix_ctx* h = new (std::nothrow) imatrix_ctx();
+    if (!h) return fail(HESS_ERR_OOM, "host allocation failed");
+    h->device = dev;
+    h->d = d;
+    cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaMalloc(&h->acc, d * sizeof(double));
+    if (e == cudaSuccess) e = cudaMemset(h->acc, 0, d * sizeof(double));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
+        cudaFree(h->acc);
+        delete h;
+        return fail(s, "imatrix_create: %s", cudaGetErrorString(e));
+    }
+    *out = h;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status imatrix_add(imatrix_t h, const void* X, int64_t n_tokens, int32_t dtype,
+                                    hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (n_tokens < 0) return fail(HESS_ERR_INVALID, "n_tokens < 0");
+    if (dtype != HESS_BF16 && dtype != HESS_F32) return fail(HESS_ERR_INVALID, "unknown dtype %d", dtype);
+    if (n_tokens == 0) return HESS_OK;
+    if (!X) return fail(HESS_ERR_INVALID, "X is NULL with n_tokens > 0");
+    if (reinterpret_cast<uintptr_t>(X) % 16 != 0) return fail(HESS_ERR_INVALID, "X is not 16-byte aligned");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    CUDA_TRY(hk::launch_colsumsq(X, dtype == HESS_F32, n_tokens, static_cast<int>(h->d), h->acc,
+                                 h->sm_count, static_cast<cudaStream_t>(stream)));
+    h->N += n_tokens;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status imatrix_read(imatrix_t h, float* out, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    CUDA_TRY(hk::launch_colsumsq_read(h->acc, out, static_cast<int>(h->d),
+                                      static_cast<cudaStream_t>(stream)));
+    return HESS_OK;
+}
+
+HESS_EXPORT int64_t imatrix_token_count(imatrix_t h) {
+    if (!h) return -1;
+    std::lock_guard<std::mutex> lk(h->mu);
+    return h->N;
+}
+
+HESS_EXPORT hess_status imatrix_reset(imatrix_t h, hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    h->N = 0;
+    CUDA_TRY(cudaMemsetAsync(h->acc, 0, h->d * sizeof(double), static_cast<cudaStream_t>(stream)));
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status imatrix_destroy(imatrix_t h) {
+    if (!h) return HESS_OK;
+    {
+        std::lock_guard<std::mutex> lk(h->mu);
+        int cur = 0;
+        cudaGetDevice(&cur);
+        cudaSetDevice(h->device);
+        cudaDeviceSynchronize();
+        cudaFree(h->acc);
+        cudaSetDevice(cur);
+    }
+    delete h;
+    return HESS_OK;
+}
+
 // ---------------------------------------------------------------- local H
 
 HESS_EXPORT hess_status local_hess_create(int64_t d, int32_t block, local_hess_t* out) {

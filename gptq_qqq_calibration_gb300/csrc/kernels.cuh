@@ -103,6 +103,13 @@ cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
                               cudaStream_t s);
 
+// dst += src over n fp64 elements (accumulator merge).
+cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_count, cudaStream_t s);
+// acc[i] += sum_t X[t][i]^2 (fp64 accumulator), X row-major [n, d], d % 8 == 0.
+cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
+                            cudaStream_t s);
+cudaError_t launch_colsumsq_read(const double* acc, float* out, int d, cudaStream_t s);
+
 // Sets the thread-local message returned by hess_last_error().
 void set_last_error(const char* msg);
 

@@ -1,0 +1,134 @@
+// Companion statistics of the calibration Hessian:
+//   * merge of two accumulators (per-device partials summed before the 2/N
+//     scale: GPTQModel PR #2979 Summary and PR #2981 Changes);
+//   * the imatrix per-column sum of squares, which NVIDIA Model-Optimizer
+//     PR #3002 ("What does this PR do?") keeps as a float32 statistic because
+//     it is not a GEMM.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace hk {
+namespace {
+
+// dst[i] += src[i] over n fp64 elements; 4 elements per thread, grid-stride.
+__global__ void __launch_bounds__(256) add_f64_kernel(double* __restrict__ dst,
+                                                      const double* __restrict__ src, size_t n) {
+    const size_t n4 = n / 4;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+        double4 a = reinterpret_cast<double4*>(dst)[i];
+        const double4 b = reinterpret_cast<const double4*>(src)[i];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+        reinterpret_cast<double4*>(dst)[i] = a;
+    }
+    for (size_t i = n4 * 4 + blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += stride)
+        dst[i] += src[i];
+}
+
+__device__ __forceinline__ float two_sum(float a, float b, float& err) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return s;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = __uint_as_float(w[k] << 16);
+        x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Thread = 8 consecutive features of one token slab.  Squares are summed in
+// fp32 chains of kChain tokens (round to nearest: unbiased), each chain is
+// folded into a compensated (hi, lo) pair, and the slab's total is added in
+// fp64 to acc.  Each warp reads 32 x 16 contiguous bytes of a token row.
+constexpr int kChain = 64;
+
+template <class T>
+__global__ void __launch_bounds__(256) colsumsq_kernel(const T* __restrict__ X, int64_t n, int d,
+                                                       int64_t slab, double* __restrict__ acc) {
+    const int f0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (f0 >= d) return;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.y) * slab;
+    const int64_t t1 = min(n, t0 + slab);
+    float hi[8] = {}, lo[8] = {};
+    for (int64_t c0 = t0; c0 < t1; c0 += kChain) {
+        const int64_t c1 = min(t1, c0 + kChain);
+        float s[8] = {};
+#pragma unroll 4
+        for (int64_t t = c0; t < c1; ++t) {
+            float x[8];
+            load8(X + t * d + f0, x);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[k], x[k], s[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float e;
+            hi[k] = two_sum(hi[k], s[k], e);
+            lo[k] = __fadd_rn(lo[k], e);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        atomicAdd(acc + f0 + k, static_cast<double>(hi[k]) + static_cast<double>(lo[k]));
+}
+
+__global__ void __launch_bounds__(256) colsumsq_read_kernel(const double* __restrict__ acc,
+                                                            float* __restrict__ out, int d) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < d) out[i] = static_cast<float>(acc[i]);
+}
+
+}  // namespace
+
+cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_count, cudaStream_t s) {
+    const size_t want = (n / 4 + 255) / 256 + 1;
+    const int grid = static_cast<int>(want < static_cast<size_t>(4 * sm_count) ? want : 4 * sm_count);
+    add_f64_kernel<<<grid, 256, 0, s>>>(dst, src, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
+                            cudaStream_t s) {
+    const int gx = (d / 8 + 255) / 256;
+    // enough token slabs for about 4 CTAs per SM, at least one chain each
+    int64_t slabs = (4LL * sm_count + gx - 1) / gx;
+    int64_t slab = (n + slabs - 1) / slabs;
+    slab = ((slab + kChain - 1) / kChain) * kChain;
+    slabs = (n + slab - 1) / slab;
+    if (slabs > 65535) {
+        slabs = 65535;
+        slab = (n + slabs - 1) / slabs;
+    }
+    const dim3 grid(gx, static_cast<unsigned>(slabs));
+    if (f32)
+        colsumsq_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), n, d, slab, acc);
+    else
+        colsumsq_kernel<__nv_bfloat16>
+            <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n, d, slab, acc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_colsumsq_read(const double* acc, float* out, int d, cudaStream_t s) {
+    colsumsq_read_kernel<<<(d + 255) / 256, 256, 0, s>>>(acc, out, d);
+    return cudaGetLastError();
+}
+
+}  // namespace hk

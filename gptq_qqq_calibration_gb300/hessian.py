@@ -25,7 +25,9 @@ __all__ = [
     "hess_pending_batches", "hess_sync", "hess_reset", "hess_set_option", "hess_destroy",
     "local_hess_create", "local_hess_add", "local_hess_read", "local_hess_token_count",
     "local_hess_sync", "local_hess_reset", "local_hess_destroy",
-    "Hessian", "LocalHessian",
+    "hess_merge", "hess_clone", "imatrix_create", "imatrix_add", "imatrix_read",
+    "imatrix_token_count", "imatrix_reset", "imatrix_destroy",
+    "Hessian", "LocalHessian", "IMatrix",
 ]
 
 _DTYPES = {torch.bfloat16: HESS_BF16, torch.float32: HESS_F32}
@@ -98,6 +100,45 @@ def hess_set_option(h: int, name: str, value: int) -> None:
 
 def hess_destroy(h: int) -> None:
     check(_lib.load().hess_destroy(h))
+
+
+def hess_merge(dst: int, src: int, stream=None) -> None:
+    check(_lib.load().hess_merge(dst, src, _stream(stream)))
+
+
+def hess_clone(src: int, stream=None) -> int:
+    h = ctypes.c_void_p()
+    check(_lib.load().hess_clone(src, ctypes.byref(h), _stream(stream)))
+    return h.value
+
+
+def imatrix_create(d: int) -> int:
+    h = ctypes.c_void_p()
+    check(_lib.load().imatrix_create(int(d), ctypes.byref(h)))
+    return h.value
+
+
+def imatrix_add(h: int, X: torch.Tensor, d: int, stream=None) -> None:
+    n, dt = _tokens_view(X, d)
+    check(_lib.load().imatrix_add(h, X.data_ptr() if n else None, n, dt, _stream(stream)))
+
+
+def imatrix_read(h: int, out: torch.Tensor, stream=None) -> None:
+    if out.dtype != torch.float32 or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 CUDA tensor")
+    check(_lib.load().imatrix_read(h, out.data_ptr(), _stream(stream)))
+
+
+def imatrix_token_count(h: int) -> int:
+    return int(_lib.load().imatrix_token_count(h))
+
+
+def imatrix_reset(h: int, stream=None) -> None:
+    check(_lib.load().imatrix_reset(h, _stream(stream)))
+
+
+def imatrix_destroy(h: int) -> None:
+    check(_lib.load().imatrix_destroy(h))
 
 
 def local_hess_create(d: int, block: int = 16) -> int:
@@ -187,6 +228,21 @@ class Hessian:
     def set_option(self, name: str, value: int) -> None:
         hess_set_option(self.handle, name, value)
 
+    def merge(self, other: "Hessian", stream=None) -> None:
+        """Add another accumulator's sums and token count into this one."""
+        hess_merge(self.handle, other.handle, stream)
+        self._release()
+        other._release()
+
+    def clone(self, stream=None) -> "Hessian":
+        """An independent copy of the sums, token count and options."""
+        h = Hessian.__new__(Hessian)
+        h.d = self.d
+        h.handle = hess_clone(self.handle, stream)
+        h._queued = []
+        self._release()
+        return h
+
     def close(self) -> None:
         if self.handle:
             hess_destroy(self.handle)
@@ -230,6 +286,41 @@ class LocalHessian:
     def close(self) -> None:
         if self.handle:
             local_hess_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class IMatrix:
+    """imatrix statistic: per-column sums of squares of the activations."""
+
+    def __init__(self, d: int):
+        self.d = int(d)
+        self.handle = imatrix_create(self.d)
+
+    def add_batch(self, X: torch.Tensor, stream=None) -> None:
+        imatrix_add(self.handle, X, self.d, stream)
+
+    def read(self, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(self.d, dtype=torch.float32, device="cuda")
+        imatrix_read(self.handle, out, stream)
+        return out
+
+    @property
+    def n_tokens(self) -> int:
+        return imatrix_token_count(self.handle)
+
+    def reset(self, stream=None) -> None:
+        imatrix_reset(self.handle, stream)
+
+    def close(self) -> None:
+        if self.handle:
+            imatrix_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

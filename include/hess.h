@@ -53,6 +53,7 @@ extern "C" {
 
 typedef struct hess_ctx* hess_t;             /* one per layer being calibrated */
 typedef struct local_hess_ctx* local_hess_t; /* one per local_hessian target */
+typedef struct imatrix_ctx* imatrix_t;       /* per-column sum of squares */
 typedef void* hess_stream_t;                 /* a cudaStream_t */
 
 /* Element type of an activation batch [P3: hessian_input_dtype]. */
@@ -159,6 +160,36 @@ hess_status hess_set_option(hess_t h, int32_t option, int64_t value);
 
 /* Free the handle (synchronises its device).  NULL is a no-op. */
 hess_status hess_destroy(hess_t h);
+
+/* Partials and copies                                                      */
+
+/* dst += src: the accumulated sums and token counts of two handles of the
+ * same width on the same device (per-device partials merged before the 2/N
+ * scale [P1 Summary; P2 Changes: "merge per-device partials"]).  Both queues
+ * are flushed on `stream` first; src is left as it was.  Enqueued on
+ * `stream`.  Errors: INVALID (NULL, same handle, widths differ),
+ * UNSUPPORTED (different devices), CUDA. */
+hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream);
+
+/* A new, independent handle holding src's sums, token count and options
+ * (shared-input dedup hands each follower a private copy of the leader's
+ * Hessian: GPTQModel PR #3052, "adopt_hessian_from").  src is flushed first.
+ * Allocates like hess_create; the copy is enqueued on `stream`. */
+hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* imatrix statistic [P3: "a per-column sum of squares, not a GEMM"]        */
+
+/* out[i] = sum over all added tokens of X[t][i]^2, accumulated in fp64 and
+ * returned as fp32.  d % 8 == 0; X row-major [n_tokens, d], 16-byte aligned,
+ * bf16 or fp32; n_tokens == 0 is a no-op. */
+hess_status imatrix_create(int64_t d, imatrix_t* out);
+hess_status imatrix_add(imatrix_t h, const void* X, int64_t n_tokens, int32_t dtype,
+                        hess_stream_t stream);
+hess_status imatrix_read(imatrix_t h, float* out, hess_stream_t stream);
+int64_t imatrix_token_count(imatrix_t h);
+hess_status imatrix_reset(imatrix_t h, hess_stream_t stream);
+hess_status imatrix_destroy(imatrix_t h);
 
 /* ------------------------------------------------------------------------ */
 /* Local (16x16 per-block) Hessian [P3: local_hessian]                      */
