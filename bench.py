@@ -304,6 +304,29 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "frac": round(fl / t / 1e12 / bf16_burst, 4), "peak_source": "bf16_tflops (burst)"}}
     h.close()
     del xs
+    # the ragged stream flushed after every batch (no queue fusion): each call
+    # reads its X and read-modify-writes the upper triangle of H
+    wl = WORKLOADS["d4096_ragged360_loguniform"].scaled(n_batches=60)
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    h = Hessian(wl.d, flush_tokens=1)
+    for X in xs:
+        h.add_batch(X)
+    torch.cuda.synchronize()
+    kern = _time_syrk(h, xs, reps=2)
+    t = kern["seconds"]
+    d = wl.d
+    tri = d * (d + 1) // 2
+    alg_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 4 * 2  # X once + fp32 upper-triangle RMW per call
+    acc_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 8 * 2  # what this library's fp64 tiles move
+    out["flush_per_call"] = {
+        "workload": wl.name + " (first 60 batches, one flush per batch)",
+        "us_per_call": round(t / len(xs) * 1e6, 2), "tflops": round(algo_flops(wl.n_tokens, d) / t / 1e12, 2),
+        "roofline": {"bound": "hbm", "achieved": round(alg_bytes / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(alg_bytes / t / 1e9 / hbm, 4),
+                     "bytes_counted": "2*n*d + 8*d(d+1)/2 per call (X once, fp32 upper-triangle read+write)",
+                     "fp64_tile_bytes_per_s_GB": round(acc_bytes / t / 1e9, 1)}}
+    h.close()
+    del xs
     # fp32-input path on the ragged d = 4096 stream (split-tf32 kernel)
     wl = WORKLOADS["d4096_ragged360_loguniform"]
     xs = [wl.batch(b, device="cuda", dtype=torch.float32) for b in range(len(wl.token_counts))]

@@ -373,6 +373,21 @@ __device__ __forceinline__ uint64_t fast_two_sum2(uint64_t a, uint64_t b, uint64
     return s;
 }
 
+// ------------------------------------------------------------ shared memory
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ global memory
 
 __device__ __forceinline__ void red_add_f64(double* p, double v) {

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) colsumsq_kernel(const T* __restrict__ X, 
     for (int64_t c0 = t0; c0 < t1; c0 += kChain) {
         const int64_t c1 = min(t1, c0 + kChain);
         float s[8] = {};
-#pragma unroll 4
+#pragma unroll 8
         for (int64_t t = c0; t < c1; ++t) {
             float x[8];
             load8(X + t * d + f0, x);
@@ -108,8 +108,8 @@ cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_coun
 cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
                             cudaStream_t s) {
     const int gx = (d / 8 + 255) / 256;
-    // enough token slabs for about 4 CTAs per SM, at least one chain each
-    int64_t slabs = (4LL * sm_count + gx - 1) / gx;
+    // enough token slabs for about 8 CTAs per SM, at least one chain each
+    int64_t slabs = (8LL * sm_count + gx - 1) / gx;
     int64_t slab = (n + slabs - 1) / slabs;
     slab = ((slab + kChain - 1) / kChain) * kChain;
     slabs = (n + slab - 1) / slab;

@@ -169,22 +169,31 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             }
             const bool diag = C.un.I == C.un.J;
             const int n_ops = diag ? 1 : 2;
-            const float4* src = reinterpret_cast<const float4*>(gbase + s * kLandBytes);
-            uint8_t* const dst = gbase + kCvtBase + c * kCvtBytes;
+            const uint32_t src = base + s * kLandBytes;
+            const uint32_t dst = base + kCvtBase + c * kCvtBytes;
             for (int op = 0; op < n_ops; ++op) {
-                float4* hi_p = reinterpret_cast<float4*>(dst + op * 2 * kOpBytes);
-                float4* lo_p = reinterpret_cast<float4*>(dst + op * 2 * kOpBytes + kOpBytes);
-                const float4* sp = src + op * (kOpBytes / 16);
-#pragma unroll 8
-                for (int i = lane; i < static_cast<int>(kOpBytes / 16); i += 32) {
-                    const float4 x = sp[i];
-                    float4 h, l;
-                    split_tf32(x.x, h.x, l.x);
-                    split_tf32(x.y, h.y, l.y);
-                    split_tf32(x.z, h.z, l.z);
-                    split_tf32(x.w, h.w, l.w);
-                    hi_p[i] = h;
-                    lo_p[i] = l;
+                const uint32_t sp = src + op * kOpBytes;
+                const uint32_t hp = dst + op * 2 * kOpBytes;
+                const uint32_t lp = hp + kOpBytes;
+                // 1,024 16-byte words per operand, 8 per lane per round, 4 rounds
+#pragma unroll 1
+                for (int r = 0; r < static_cast<int>(kOpBytes / 16 / 256); ++r) {
+                    uint4 x[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[k] = lds128(sp + ((r * 8 + k) * 32 + lane) * 16);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = ((r * 8 + k) * 32 + lane) * 16;
+                        float h0, h1, h2, h3, l0, l1, l2, l3;
+                        split_tf32(__uint_as_float(x[k].x), h0, l0);
+                        split_tf32(__uint_as_float(x[k].y), h1, l1);
+                        split_tf32(__uint_as_float(x[k].z), h2, l2);
+                        split_tf32(__uint_as_float(x[k].w), h3, l3);
+                        sts128(hp + off, make_uint4(__float_as_uint(h0), __float_as_uint(h1),
+                                                    __float_as_uint(h2), __float_as_uint(h3)));
+                        sts128(lp + off, make_uint4(__float_as_uint(l0), __float_as_uint(l1),
+                                                    __float_as_uint(l2), __float_as_uint(l3)));
+                    }
                 }
             }
             // generic-proxy writes (and reads of the landing slot) must be
