@@ -21,7 +21,9 @@ Readings (the pages do not spell these out):
   * error of column i: (w_i - q_i) / U_ii, propagated as
     W[:, j] -= err * U_ij for j > i (within the block at once, beyond the
     block after it);
-  * loss = sum over columns and rows of (w - q)^2 / U_ii^2 / 2;
+  * loss = sum over columns and rows of (w - q)^2 / U_ii^2 / 2, and the
+    reported average divides that sum by the Hessian's token count (same
+    page, "Quantizer API and results");
   * "Whole-row and grouped weight quantization" (same page): whole-row
     (group_size = -1) codes are signed 4-bit with one symmetric scale per
     row, s = max|w_row| / 7, q = clamp(round(w / s), -8, 7); grouped
@@ -65,12 +67,15 @@ def quantize_column(w, s, grouped: bool, dtype=np.float64):
     return (s * q).astype(dtype), q
 
 
-def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.float64, U=None):
-    """Run steps 1-5.  Returns dict(Wq, scales, damp, loss, U, dead).
+def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.float64, U=None,
+                  n_tokens=None):
+    """Run steps 1-5.  Returns dict(Wq, codes, scales, damp, loss, avg_loss, U, dead).
 
     `dtype` is the arithmetic of steps 5 (float64 by default; float32 to take
     the quantization decisions in the kernel's precision).  `U` may be given
-    to reuse a factor computed elsewhere.
+    to reuse a factor computed elsewhere.  `codes` are the signed 4-bit
+    values c with Wq = scale * c (grouped codes stored centered: c = q - 8).
+    `avg_loss` is loss / n_tokens when n_tokens is given and positive.
     """
     H = np.array(H, dtype=np.float64)
     W = np.array(W, dtype=np.float64)  # step 1: working copy
@@ -99,6 +104,7 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
     if not grouped:
         scales[:, 0] = _scale(np.max(np.abs(Ww), axis=1), 7.0)
     Wq = np.zeros_like(Ww)
+    codes = np.zeros(Ww.shape, dtype=np.int8)
     loss = 0.0
     # step 5: blocks of 128 columns
     for b0 in range(0, d, BLOCK):
@@ -109,8 +115,9 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
         s = scales[:, b0 // BLOCK if grouped else 0]
         for i in range(b0, b1):
             w = Ww[:, i]
-            wq, _ = quantize_column(w, s, grouped, dtype)
+            wq, q = quantize_column(w, s, grouped, dtype)
             Wq[:, i] = wq
+            codes[:, i] = (q - 8) if grouped else q
             dii = Uw[i, i]
             err = ((w - wq) / dii).astype(dtype)
             loss += float(np.sum(((w - wq).astype(np.float64) / float(dii)) ** 2) / 2.0)
@@ -118,4 +125,6 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
             Err[:, i - b0] = err
         if b1 < d:
             Ww[:, b1:] -= (Err @ Uw[b0:b1, b1:]).astype(dtype)
-    return {"Wq": Wq, "scales": scales, "damp": damp, "loss": loss, "U": U, "dead": dead}
+    avg_loss = loss / n_tokens if n_tokens else None
+    return {"Wq": Wq, "codes": codes, "scales": scales, "damp": damp, "loss": loss,
+            "avg_loss": avg_loss, "U": U, "dead": dead}

@@ -165,3 +165,15 @@ def test_pins_catch_planted_mistakes(kind):
         except (AssertionError, np.linalg.LinAlgError):
             failed += 1
     assert failed, kind
+
+
+def test_codes_and_average_loss():
+    """Wq = scale * code with codes in [-8, 7]; the average loss divides the
+    summed loss by the token count."""
+    H, W = _problem(seed=9)
+    for group in (128, -1):
+        res = go.gptq_quantize(H, W, 0.01, group, n_tokens=1000)
+        s = np.repeat(res["scales"], 128, axis=1) if group == 128 else res["scales"]
+        np.testing.assert_array_equal(res["Wq"], s * res["codes"])
+        assert res["codes"].min() >= -8 and res["codes"].max() <= 7
+        assert res["avg_loss"] == res["loss"] / 1000
