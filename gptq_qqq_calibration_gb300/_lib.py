@@ -1,4 +1,4 @@
-"""ctypes loader for ``libgptq_hess.so`` and the prototypes of ``include/hess.h``.
+"""ctypes loader for ``libgptq_hess.so`` and the prototypes of ``include/*.h``.
 
 Loading never falls back to anything: if the library is missing the caller
 gets a RuntimeError naming the build step.
@@ -13,16 +13,17 @@ import threading
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgptq_hess.so")
 
 HESS_BF16, HESS_F32 = 0, 1
-HESS_OK, HESS_ERR_INVALID, HESS_ERR_UNSUPPORTED, HESS_ERR_OOM, HESS_ERR_CUDA, HESS_ERR_TIMEOUT = range(6)
+(HESS_OK, HESS_ERR_INVALID, HESS_ERR_UNSUPPORTED, HESS_ERR_OOM, HESS_ERR_CUDA, HESS_ERR_TIMEOUT,
+ HESS_ERR_NOT_PD) = range(7)
 STATUS_NAMES = {0: "HESS_OK", 1: "HESS_ERR_INVALID", 2: "HESS_ERR_UNSUPPORTED", 3: "HESS_ERR_OOM",
-                4: "HESS_ERR_CUDA", 5: "HESS_ERR_TIMEOUT"}
+                4: "HESS_ERR_CUDA", 5: "HESS_ERR_TIMEOUT", 6: "HESS_ERR_NOT_PD"}
 OPTIONS = {"flush_tokens": 1, "max_pending": 2, "chunk_tokens": 3, "wait_timeout_ns": 4,
            "split_k": 5, "grid": 6, "pair_kernel": 7}
 
 _vp, _i32, _i64, _f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
 _fp = ctypes.POINTER(ctypes.c_float)
 
-# name -> (restype, argtypes); mirrors include/hess.h
+# name -> (restype, argtypes); mirrors include/hess.h and include/gptq.h
 PROTOTYPES = {
     "hess_create": (_i32, [_i64, ctypes.POINTER(_vp)]),
     "hess_add_batch": (_i32, [_vp, _vp, _i64, _i32, _vp]),
@@ -51,6 +52,12 @@ PROTOTYPES = {
     "local_hess_reset": (_i32, [_vp, _vp]),
     "local_hess_destroy": (_i32, [_vp]),
     "local_hess_compute_noalloc": (_i32, [_vp, _i64, _i64, _i32, _i32, _vp, _vp]),
+    "gptq_create": (_i32, [_i64, _i64, ctypes.POINTER(_vp)]),
+    "gptq_prepare": (_i32, [_vp, _vp, _i64, _f64, _vp, _fp]),
+    "gptq_prepare_hess": (_i32, [_vp, _vp, _f64, _vp, _fp]),
+    "gptq_read_factor": (_i32, [_vp, _vp, _vp]),
+    "gptq_quantize": (_i32, [_vp, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _vp, ctypes.POINTER(_f64)]),
+    "gptq_destroy": (_i32, [_vp]),
     "hess_last_error": (ctypes.c_char_p, []),
     "hess_abi_version": (_i32, []),
 }

@@ -157,3 +157,21 @@ WORKLOADS = {
     # local_hessian: 8 updates of 32,768 tokens, 1 % Student-t(3) channels.
     "local_d4096_8x32768": Workload("local_d4096_8x32768", 4096, (32768,) * 8, "student_t", 5, local=True),
 }
+
+
+def make_weight(rows: int, d: int, seed: int, *, dtype: torch.dtype = torch.float32, device="cpu") -> torch.Tensor:
+    """A ``[rows, d]`` linear-layer weight (output channel by input column).
+
+    Entries are N(0, 0.02^2), the usual initialisation scale of transformer
+    projections, with 1 % of the input columns scaled by 8 (salient columns)
+    so that group maxima differ across groups.  Drawn in fp32, rounded once
+    to ``dtype``.
+    """
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    w = 0.02 * torch.randn((rows, d), generator=g, device=dev, dtype=torch.float32)
+    rng = np.random.default_rng(20_000 + int(seed))
+    cols = rng.permutation(d)[: max(1, d // 100)]
+    w[:, torch.from_numpy(cols).to(dev)] *= 8.0
+    return w.to(dtype).contiguous()

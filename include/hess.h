@@ -68,7 +68,8 @@ typedef enum {
     HESS_ERR_UNSUPPORTED = 2, /* valid but not supported (d % 8 != 0, block != 16, ...) */
     HESS_ERR_OOM = 3,         /* device or host allocation failed (create only) */
     HESS_ERR_CUDA = 4,        /* a CUDA call failed; see hess_last_error() */
-    HESS_ERR_TIMEOUT = 5      /* a device-side wait ran out; results are invalid */
+    HESS_ERR_TIMEOUT = 5,     /* a device-side wait ran out; results are invalid */
+    HESS_ERR_NOT_PD = 6       /* gptq_prepare: the damped Hessian has no fp32 Cholesky factor */
 } hess_status;
 
 /* Options for hess_set_option. */

@@ -69,13 +69,14 @@ def quantize_column(w, s, grouped: bool, dtype=np.float64):
 
 def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.float64, U=None,
                   n_tokens=None):
-    """Run steps 1-5.  Returns dict(Wq, codes, scales, damp, loss, avg_loss, U, dead).
+    """Run steps 1-5.  Returns dict(Wq, codes, scales, damp, loss, avg_loss, U, dead, Wpre).
 
     `dtype` is the arithmetic of steps 5 (float64 by default; float32 to take
     the quantization decisions in the kernel's precision).  `U` may be given
     to reuse a factor computed elsewhere.  `codes` are the signed 4-bit
     values c with Wq = scale * c (grouped codes stored centered: c = q - 8).
     `avg_loss` is loss / n_tokens when n_tokens is given and positive.
+    `Wpre[:, i]` is the value column i held when it was quantized.
     """
     H = np.array(H, dtype=np.float64)
     W = np.array(W, dtype=np.float64)  # step 1: working copy
@@ -105,6 +106,7 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
         scales[:, 0] = _scale(np.max(np.abs(Ww), axis=1), 7.0)
     Wq = np.zeros_like(Ww)
     codes = np.zeros(Ww.shape, dtype=np.int8)
+    Wpre = np.zeros_like(Ww)
     loss = 0.0
     # step 5: blocks of 128 columns
     for b0 in range(0, d, BLOCK):
@@ -115,6 +117,7 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
         s = scales[:, b0 // BLOCK if grouped else 0]
         for i in range(b0, b1):
             w = Ww[:, i]
+            Wpre[:, i] = w
             wq, q = quantize_column(w, s, grouped, dtype)
             Wq[:, i] = wq
             codes[:, i] = (q - 8) if grouped else q
@@ -127,4 +130,4 @@ def gptq_quantize(H, W, damp_percent: float, group_size: int = 128, dtype=np.flo
             Ww[:, b1:] -= (Err @ Uw[b0:b1, b1:]).astype(dtype)
     avg_loss = loss / n_tokens if n_tokens else None
     return {"Wq": Wq, "codes": codes, "scales": scales, "damp": damp, "loss": loss,
-            "avg_loss": avg_loss, "U": U, "dead": dead}
+            "avg_loss": avg_loss, "U": U, "dead": dead, "Wpre": Wpre}

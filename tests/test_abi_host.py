@@ -1,10 +1,11 @@
 """Host-side checks of the C ABI (no GPU needed).
 
-The library must load, export every function ``include/hess.h`` declares,
-and reject invalid arguments before any CUDA call.
+The library must load, export every function ``include/*.h`` declares, and
+reject invalid arguments before any CUDA call.
 """
 
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -25,14 +26,15 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(p).read() for p in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("hess_create", "hess_add_batch", "hess_materialize", "local_hess_add", "hess_destroy"):
+    for n in ("hess_create", "hess_add_batch", "hess_materialize", "local_hess_add", "hess_destroy",
+              "gptq_create", "gptq_prepare", "gptq_quantize"):
         assert n in names
 
 
@@ -68,6 +70,24 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.local_hess_create(40, 16, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED
     assert lib.local_hess_add(None, None, 0, 16, 16, 0, None) == HESS_ERR_INVALID
     assert lib.local_hess_destroy(None) == 0
+    g = ctypes.c_void_p()
+    assert lib.gptq_create(0, 4, ctypes.byref(g)) == HESS_ERR_INVALID
+    assert lib.gptq_create(256, -1, ctypes.byref(g)) == HESS_ERR_INVALID
+    assert lib.gptq_create(200, 4, ctypes.byref(g)) == HESS_ERR_UNSUPPORTED
+    assert b"multiple of 128" in lib.hess_last_error()
+    assert lib.gptq_create(256, 4, None) == HESS_ERR_INVALID
+    assert lib.gptq_prepare(None, None, 0, 0.01, None, None) == HESS_ERR_INVALID
+    assert lib.gptq_prepare_hess(None, None, 0.01, None, None) == HESS_ERR_INVALID
+    assert lib.gptq_read_factor(None, None, None) == HESS_ERR_INVALID
+    assert lib.gptq_quantize(None, None, 0, 0, 128, None, None, None, None, None) == HESS_ERR_INVALID
+    assert lib.gptq_destroy(None) == 0
+
+
+def test_status_codes_match_header():
+    from gptq_qqq_calibration_gb300 import _lib
+    text = open(HEADER).read()
+    enum = dict((k, int(v)) for k, v in re.findall(r"(HESS_(?:OK|ERR_\w+))\s*=\s*(\d+)", text))
+    assert enum == {v: k for k, v in _lib.STATUS_NAMES.items()}
 
 
 def test_injected_allocation_failure_reports_oom():

@@ -177,3 +177,7 @@ def test_codes_and_average_loss():
         np.testing.assert_array_equal(res["Wq"], s * res["codes"])
         assert res["codes"].min() >= -8 and res["codes"].max() <= 7
         assert res["avg_loss"] == res["loss"] / 1000
+        # Wpre is what each column held when quantized: the code is its
+        # rounded quotient by the scale
+        q = np.clip(np.rint(res["Wpre"] / s), -8, 7)
+        np.testing.assert_array_equal(q, res["codes"])
