@@ -40,10 +40,9 @@ constexpr int kNB = 128;          // column block of the factorization and of st
 constexpr int kLd = kNB + 1;      // padded row of the diagonal-block tiles
 constexpr int kGemmLd = 132;      // padded row of the GEMM k-slices
 constexpr int kGemmCLowerTiles = 1;
-constexpr int kPotrfThreads = 512;
+constexpr int kPotrfThreads = 256;
 constexpr int kBlockThreads = 128;
 constexpr int kSuper = 4;          // blocks per lazy super-block of step 5
-constexpr size_t kPotrfSmem = 2 * kNB * kLd * sizeof(float);
 constexpr size_t kBlockSmem = kNB * kNB * sizeof(float);
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -109,89 +108,246 @@ __global__ void gq_rotate_in_kernel(const float* __restrict__ H, float* __restri
 // ------------------------------------------------------------- step 4
 
 // Factor the diagonal block k of F in place (F = L L^T, lower) and write
-// inv(L_kk) to Dinv.  A pivot that is not a positive finite number sets
-// status bit 1 and is replaced by 1 so the kernel still ends normally.
-__global__ void __launch_bounds__(kPotrfThreads) gq_potrf_kernel(float* __restrict__ F, int d, int k,
+// inv(L_kk) to Dinv.  The 128 columns go in sub-panels of kSub:
+//   1. one warp factors the kSub x kSub diagonal sub-block in registers
+//      (lane i holds row i; pivots and column entries travel by shuffle) and
+//      inverts it by forward substitution (lane j holds column j of the
+//      inverse).  The unrolled code of this step is kept small enough to stay
+//      in the instruction cache: with 32 columns it was fetch-bound;
+//   2. all warps solve the rows below the sub-panel, L21 = A21 inv(L11)^T,
+//      in 4 x 4 register tiles;
+//   3. all warps apply the rank-kSub update to the rows and columns after it.
+// The 128 x 128 inverse is built alongside, right-looking by block columns:
+// with B = I, block row p becomes X_p = Y_p B_p (Y_p the sub-block inverse)
+// once its sub-panel is factored, and every later block row then takes
+// B_i -= L_ip X_p; these steps share the sub-panel loop's barriers.
+// A pivot that is not a positive finite number sets status bit 1 and is
+// replaced by 1 so the kernel still ends normally.
+constexpr int kSub = 16;             // sub-panel width (one warp's register factor)
+constexpr int kSubT = kSub / 4;       // 4-wide tiles across a sub-panel
+constexpr int kLtLd = kNB + 4;        // transposed panel rows (float4-aligned)
+constexpr int kYtLd = kSub + 4;       // transposed sub-block inverse rows
+constexpr size_t kPotrfFloats =
+    2 * kNB * kLd + kSub * kLtLd + kSub * kYtLd + kNB;
+constexpr size_t kPotrfSmem = kPotrfFloats * sizeof(float);
+
+__global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __restrict__ F, int d, int k,
                                                                  float* __restrict__ Dinv,
                                                                  int* __restrict__ status) {
-    extern __shared__ float sm[];
-    float* S = sm;               // [kNB][kLd]: the block, then L
-    float* X = sm + kNB * kLd;   // [kNB][kLd]: inv(L)
-    const int tid = threadIdx.x;
+    extern __shared__ __align__(16) float sm[];
+    float* S = sm;                  // [kNB][kLd]: the block, then L
+    float* Xs = S + kNB * kLd;      // [kNB][kLd]: inv(L)
+    float* Lt = Xs + kNB * kLd;     // [kSub][kLtLd]: L21 of the current sub-panel, transposed
+    float* Yt = Lt + kSub * kLtLd;  // [kSub][kYtLd]: inverse of the current sub-block, transposed
+    float* rl = Yt + kSub * kYtLd;  // [kNB]: 1 / L_ii
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float* blk = F + static_cast<size_t>(k) * kNB * d + static_cast<size_t>(k) * kNB;
-    for (int e = tid; e < kNB * kNB; e += kPotrfThreads) {
-        const int i = e >> 7, j = e & (kNB - 1);
-        S[i * kLd + j] = j <= i ? blk[static_cast<size_t>(i) * d + j] : 0.0f;
-        X[i * kLd + j] = 0.0f;
+    constexpr int kVecPerThread = kNB * kNB / 4 / kPotrfThreads;
+    {
+        float4 v[kVecPerThread];  // every load in flight before the first store
+#pragma unroll
+        for (int it = 0; it < kVecPerThread; ++it) {
+            const int e4 = tid + it * kPotrfThreads, i = e4 >> 5, j = (e4 & 31) * 4;
+            v[it] = *reinterpret_cast<const float4*>(blk + static_cast<size_t>(i) * d + j);
+        }
+#pragma unroll
+        for (int it = 0; it < kVecPerThread; ++it) {
+            const int e4 = tid + it * kPotrfThreads, i = e4 >> 5, j = (e4 & 31) * 4;
+            const float x[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                S[i * kLd + j + u] = j + u <= i ? x[u] : 0.0f;
+                Xs[i * kLd + j + u] = 0.0f;
+            }
+        }
     }
     __syncthreads();
-
-    // Right-looking, one column per step.  Thread (row = tid % 128,
-    // part = tid / 128) updates columns c = j+1+part, j+5+part, ... of its row.
-    const int row = tid & (kNB - 1), part = tid >> 7;
     bool bad = false;
-    for (int j = 0; j < kNB; ++j) {
-        float p = S[j * kLd + j];
-        if (!(p > 0.0f) || !(p < INFINITY)) {
-            bad = true;
-            p = 1.0f;
-        }
-        const float l = sqrtf(p);
-        if (part == 0 && row > j) S[row * kLd + j] = __fdiv_rn(S[row * kLd + j], l);
-        __syncthreads();  // column j scaled; every thread has read the pivot
-        if (part == 0 && row == j) S[j * kLd + j] = l;
-        if (row > j) {
-            // Four elements per round, all loads before the stores (the
-            // compiler cannot prove the stores miss the next loads).
-            const float lr = S[row * kLd + j];
-            int c = j + 1 + part;
-            for (; c + 12 <= row; c += 16) {
-                const float a0 = S[row * kLd + c], a1 = S[row * kLd + c + 4];
-                const float a2 = S[row * kLd + c + 8], a3 = S[row * kLd + c + 12];
-                const float b0 = S[c * kLd + j], b1 = S[(c + 4) * kLd + j];
-                const float b2 = S[(c + 8) * kLd + j], b3 = S[(c + 12) * kLd + j];
-                S[row * kLd + c] = fmaf(-lr, b0, a0);
-                S[row * kLd + c + 4] = fmaf(-lr, b1, a1);
-                S[row * kLd + c + 8] = fmaf(-lr, b2, a2);
-                S[row * kLd + c + 12] = fmaf(-lr, b3, a3);
+    for (int p = 0; p < kNB / kSub; ++p) {
+        const int P = p * kSub;
+        if (warp == 0) {
+            // Lanes kSub..31 take part in the shuffles only.
+            const bool in = lane < kSub;
+            float dv[kSub];
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) dv[c] = in ? S[(P + lane) * kLd + P + c] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) {
+                float piv = __shfl_sync(kFull, dv[j], j);
+                if (!(piv > 0.0f) || !(piv < INFINITY)) {
+                    bad = true;
+                    piv = 1.0f;
+                }
+                // 1/sqrt by the hardware estimate and one Newton step,
+                // y <- y (1.5 - 0.5 x y^2): the pivot chain is the
+                // sequential path of the whole factorization.
+                float il = rsqrtf(piv);
+                il = __fmul_rn(il, fmaf(-0.5f * piv * il, il, 1.5f));
+                const float l = __fmul_rn(piv, il);
+                if (lane == j) dv[j] = l;
+                else if (lane > j) dv[j] = __fmul_rn(dv[j], il);
+                if (lane == 0) rl[P + j] = il;
+#pragma unroll
+                for (int c = 0; c < kSub; ++c) {
+                    if (c > j) {  // resolved at compile time
+                        const float lc = __shfl_sync(kFull, dv[j], c);
+                        if (lane >= c) dv[c] = fmaf(-dv[j], lc, dv[c]);
+                    }
+                }
             }
-            for (; c <= row; c += 4) S[row * kLd + c] = fmaf(-lr, S[c * kLd + j], S[row * kLd + c]);
+            if (in) {
+#pragma unroll
+                for (int c = 0; c < kSub; ++c) S[(P + lane) * kLd + P + c] = c <= lane ? dv[c] : 0.0f;
+            }
+            __syncwarp();
+            // Column `lane` of the sub-block inverse: solve L y = e_lane.
+            float acc[kSub];
+#pragma unroll
+            for (int i = 0; i < kSub; ++i) acc[i] = i == lane ? 1.0f : 0.0f;
+#pragma unroll
+            for (int m = 0; m < kSub; ++m) {
+                acc[m] = __fmul_rn(acc[m], rl[P + m]);
+#pragma unroll
+                for (int i = 0; i < kSub; ++i)
+                    if (i > m) acc[i] = fmaf(-S[(P + i) * kLd + P + m], acc[m], acc[i]);
+            }
+            if (in) {
+#pragma unroll
+                for (int i = 0; i < kSub; ++i) {
+                    Xs[(P + i) * kLd + P + lane] = acc[i];  // Y[i][lane] (0 for i < lane)
+                    Yt[lane * kYtLd + i] = acc[i];           // Yt[m][c] = Y[c][m]
+                }
+            }
+        }
+        __syncthreads();
+        const int R0 = P + kSub;  // first row after the sub-panel
+        const int nb = kNB - R0;
+        // 2. In registers: tiles of L21 = A21 Y^T (threads [0, n2)) and tiles of
+        //    block row p of the inverse, X_p,j = Y B_p,j for the columns before
+        //    the sub-panel (threads [n2, n2 + P)); B_p,j holds I - sum L X there.
+        const int n2 = (nb / 4) * kSubT;
+        int mode = 0, r0 = 0, c0 = 0;
+        float a2[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) a2[t][u] = 0.0f;
+        if (tid < n2) {
+            mode = 1;
+            r0 = R0 + 4 * (tid / kSubT);
+            c0 = 4 * (tid % kSubT);
+            for (int m = 0; m < c0 + 4; ++m) {  // Y[c][m] = 0 for m > c
+                const float4 y = *reinterpret_cast<const float4*>(&Yt[m * kYtLd + c0]);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float av = S[(r0 + t) * kLd + P + m];
+                    a2[t][0] = fmaf(av, y.x, a2[t][0]);
+                    a2[t][1] = fmaf(av, y.y, a2[t][1]);
+                    a2[t][2] = fmaf(av, y.z, a2[t][2]);
+                    a2[t][3] = fmaf(av, y.w, a2[t][3]);
+                }
+            }
+        } else if (tid < n2 + P) {
+            mode = 2;
+            const int q = tid - n2;
+            r0 = 4 * (q % kSubT);  // row within block row p
+            c0 = 4 * (q / kSubT);  // column < P
+            for (int m = 0; m < r0 + 4; ++m) {  // Y[t][m] = 0 for m > t
+                const float4 y = *reinterpret_cast<const float4*>(&Yt[m * kYtLd + r0]);
+                const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float bv = Xs[(P + m) * kLd + c0 + u];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) a2[t][u] = fmaf(yv[t], bv, a2[t][u]);
+                }
+            }
+        }
+        __syncthreads();  // every read of A21 and B_p is done
+        if (mode == 1) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) S[(r0 + t) * kLd + P + c0 + u] = a2[t][u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<float4*>(&Lt[(c0 + u) * kLtLd + (r0 - R0)]) =
+                    make_float4(a2[0][u], a2[1][u], a2[2][u], a2[3][u]);
+        } else if (mode == 2) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) Xs[(P + r0 + t) * kLd + c0 + u] = a2[t][u];
+        }
+        __syncthreads();
+        if (nb == 0) break;
+        // 3. On 4 x 4 tiles: A22 -= L21 L21^T at or below the diagonal
+        //    (idx < n3), and B_i,j -= L_ip X_p,j for the rows after the
+        //    sub-panel and the columns up to its end (the rest).
+        const int nt = nb / 4;
+        const int n3 = nt * (nt + 1) / 2;
+        const int ct = (P + kSub) / 4;
+        for (int idx = tid; idx < n3 + nt * ct; idx += kPotrfThreads) {
+            float a3[4][4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) a3[t][u] = 0.0f;
+            if (idx < n3) {
+                int ta = static_cast<int>((sqrtf(8.0f * idx + 1.0f) - 1.0f) * 0.5f);
+                while (ta * (ta + 1) / 2 > idx) --ta;
+                while ((ta + 1) * (ta + 2) / 2 <= idx) ++ta;
+                const int tb = idx - ta * (ta + 1) / 2;  // 0 <= tb <= ta < nt
+#pragma unroll 4
+                for (int m = 0; m < kSub; ++m) {
+                    const float4 x = *reinterpret_cast<const float4*>(&Lt[m * kLtLd + 4 * ta]);
+                    const float4 y = *reinterpret_cast<const float4*>(&Lt[m * kLtLd + 4 * tb]);
+                    const float xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) a3[t][u] = fmaf(xv[t], yv[u], a3[t][u]);
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) S[(R0 + 4 * ta + t) * kLd + R0 + 4 * tb + u] -= a3[t][u];
+            } else {
+                const int q = idx - n3;
+                const int ta = q / ct, tb = q % ct;  // row tile after R0, column tile
+#pragma unroll 4
+                for (int m = 0; m < kSub; ++m) {
+                    const float4 x = *reinterpret_cast<const float4*>(&Lt[m * kLtLd + 4 * ta]);
+                    const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float bv = Xs[(P + m) * kLd + 4 * tb + u];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) a3[t][u] = fmaf(xv[t], bv, a3[t][u]);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) Xs[(R0 + 4 * ta + t) * kLd + 4 * tb + u] -= a3[t][u];
+            }
         }
         __syncthreads();
     }
     if (bad && tid == 0) atomicOr(status, 1);
-    __shared__ float rdiag[kNB];
-    if (tid < kNB) rdiag[tid] = __frcp_rn(S[tid * kLd + tid]);
-    __syncthreads();
 
-    // inv(L) by forward substitution: column j = tid / 4 is solved by four
-    // threads (consecutive lanes) that split each dot product.
-    {
-        const int col = tid >> 2, q = tid & 3;
-        const int first = (tid >> 5) * 8;  // smallest column of this warp
-        for (int i = first; i < kNB; ++i) {
-            float a0 = 0.0f, a1 = 0.0f;
-            if (i > col) {
-                int m = col + q;
-                for (; m + 4 < i; m += 8) {
-                    a0 = fmaf(S[i * kLd + m], X[m * kLd + col], a0);
-                    a1 = fmaf(S[i * kLd + m + 4], X[(m + 4) * kLd + col], a1);
-                }
-                if (m < i) a0 = fmaf(S[i * kLd + m], X[m * kLd + col], a0);
-            }
-            float acc = a0 + a1;
-            acc += __shfl_xor_sync(kFull, acc, 1);
-            acc += __shfl_xor_sync(kFull, acc, 2);
-            if (i >= col && q == 0) X[i * kLd + col] = ((i == col ? 1.0f : 0.0f) - acc) * rdiag[i];
-            __syncwarp();
-        }
-    }
-    __syncthreads();
     float* inv = Dinv + static_cast<size_t>(k) * kNB * kNB;
-    for (int e = tid; e < kNB * kNB; e += kPotrfThreads) {
-        const int i = e >> 7, j = e & (kNB - 1);
-        blk[static_cast<size_t>(i) * d + j] = S[i * kLd + j];
-        inv[e] = X[i * kLd + j];
+#pragma unroll 4
+    for (int it = 0; it < kVecPerThread; ++it) {
+        const int e4 = tid + it * kPotrfThreads, i = e4 >> 5, j = (e4 & 31) * 4;
+        float l[4], x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            l[u] = j + u <= i ? S[i * kLd + j + u] : 0.0f;
+            x[u] = j + u <= i ? Xs[i * kLd + j + u] : 0.0f;
+        }
+        *reinterpret_cast<float4*>(blk + static_cast<size_t>(i) * d + j) = make_float4(l[0], l[1], l[2], l[3]);
+        *reinterpret_cast<float4*>(inv + i * kNB + j) = make_float4(x[0], x[1], x[2], x[3]);
     }
 }
 
@@ -203,6 +359,8 @@ struct GemmArgs {
     float alpha;
     int beta;  // 0: C = alpha AB; 1: C = C + alpha AB
     int flags;
+    long long sA, sB, sC;  // element strides between the problems of a batch (grid z)
+    int diag_step;         // lower-tile test of problem z: skip tiles with n0 > m0 + z * diag_step
 };
 
 // C = beta C + alpha A op(B) in fp32 (FMA chains along k, one rounding per
@@ -215,14 +373,17 @@ struct GemmArgs {
 template <bool kTransB>
 __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
     const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
-    if ((g.flags & kGemmCLowerTiles) && n0 > m0) return;
+    if ((g.flags & kGemmCLowerTiles) && n0 > m0 + static_cast<int>(blockIdx.z) * g.diag_step) return;
+    const float* Ab = g.A + blockIdx.z * g.sA;
+    const float* Bb = g.B + blockIdx.z * g.sB;
+    float* Cb = g.C + blockIdx.z * g.sC;
     __shared__ __align__(16) float As[2][8][kGemmLd];
     __shared__ __align__(16) float Bs[2][8][kGemmLd];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int r_row = tid >> 1, r_col = (tid & 1) * 4;      // row-of-8 loader (A, transposed B)
     const int b_k = tid >> 5, b_n = (tid & 31) * 4;         // plain B loader
     const bool a_ok = m0 + r_row < g.M;
-    const float* a_src = g.A + static_cast<size_t>(a_ok ? m0 + r_row : 0) * g.lda + r_col;
+    const float* a_src = Ab + static_cast<size_t>(a_ok ? m0 + r_row : 0) * g.lda + r_col;
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -234,9 +395,9 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
         // Plain loads: C may alias A or B, so the read-only path is not used.
         ra = a_ok ? *reinterpret_cast<const float4*>(a_src + k0) : make_float4(0.f, 0.f, 0.f, 0.f);
         if (kTransB)
-            rb = *reinterpret_cast<const float4*>(g.B + static_cast<size_t>(n0 + r_row) * g.ldb + k0 + r_col);
+            rb = *reinterpret_cast<const float4*>(Bb + static_cast<size_t>(n0 + r_row) * g.ldb + k0 + r_col);
         else
-            rb = *reinterpret_cast<const float4*>(g.B + static_cast<size_t>(k0 + b_k) * g.ldb + n0 + b_n);
+            rb = *reinterpret_cast<const float4*>(Bb + static_cast<size_t>(k0 + b_k) * g.ldb + n0 + b_n);
     };
     auto store = [&](int buf) {
         As[buf][r_col + 0][r_row] = ra.x;
@@ -284,7 +445,7 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
         if (m >= g.M) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float4* cp = reinterpret_cast<float4*>(g.C + static_cast<size_t>(m) * g.ldc + n0 + h * 64 + tx * 4);
+            float4* cp = reinterpret_cast<float4*>(Cb + static_cast<size_t>(m) * g.ldc + n0 + h * 64 + tx * 4);
             float4 o = make_float4(g.alpha * acc[i][h * 4 + 0], g.alpha * acc[i][h * 4 + 1],
                                    g.alpha * acc[i][h * 4 + 2], g.alpha * acc[i][h * 4 + 3]);
             if (g.beta) {
@@ -502,10 +663,11 @@ hess_status gq_fail(hess_status s, const char* fmt, ...) {
 
 template <bool kTransB>
 cudaError_t gemm(const float* A, int lda, const float* B, int ldb, float* C, int ldc, int M, int N, int K,
-                 float alpha, int beta, int flags, cudaStream_t s) {
-    if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
-    GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, flags};
-    const dim3 grid(N / 128, (M + 127) / 128);
+                 float alpha, int beta, int flags, cudaStream_t s, int batch = 1, long long sA = 0,
+                 long long sB = 0, long long sC = 0, int diag_step = 0) {
+    if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return cudaSuccess;
+    GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, flags, sA, sB, sC, diag_step};
+    const dim3 grid(N / 128, (M + 127) / 128, batch);
     gq_gemm_kernel<kTransB><<<grid, 256, 0, s>>>(g);
     return cudaGetLastError();
 }
@@ -535,6 +697,9 @@ struct gptq_ctx {
     float* damp32 = nullptr;
     double* loss = nullptr;
     int* status = nullptr;
+    float* Mk = nullptr;             // (d - 128) x 128: L_ik inv(L_kk) of one step
+    cudaStream_t side = nullptr;     // inverse block rows, alongside the Cholesky
+    cudaEvent_t ev_fork = nullptr, ev_panel = nullptr, ev_side = nullptr;
     bool prepared = false;
     int64_t n_tokens = 0;
 };
@@ -561,6 +726,11 @@ void gq_free(gptq_ctx* g) {
     cudaFree(g->damp32);
     cudaFree(g->loss);
     cudaFree(g->status);
+    cudaFree(g->Mk);
+    if (g->side) cudaStreamDestroy(g->side);
+    if (g->ev_fork) cudaEventDestroy(g->ev_fork);
+    if (g->ev_panel) cudaEventDestroy(g->ev_panel);
+    if (g->ev_side) cudaEventDestroy(g->ev_side);
 }
 
 bool misaligned(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 != 0; }
@@ -576,7 +746,19 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
     GQ_TRY(cudaGetLastError());
     gq_rotate_in_kernel<<<stride_grid(dd / 4, g->sm_count), 256, 0, s>>>(H, g->F, d, g->dead, g->damp64);
     GQ_TRY(cudaGetLastError());
-    // Blocked right-looking Cholesky of F = J H J.
+    // Blocked right-looking Cholesky of F = J H J on `s`, and alongside it on
+    // the side stream the block rows of inv(L): with B = I - (strictly lower
+    // sums), X_k = inv(L_kk) B_k, and after step k every later block row
+    // takes B_i -= (L_ik inv(L_kk)) B_k.  The factors M_k = L_ik inv(L_kk)
+    // are formed from the finished panel, so only the Cholesky itself is on
+    // the critical path; the products X_k = inv(L_kk) B_k run at the end in
+    // one batched launch.  The side stream reads only finished panels and
+    // inv(L_kk) and writes only X and M_k (reused in its own order).
+    GQ_TRY(cudaMemsetAsync(g->X, 0, dd * sizeof(float), s));
+    gq_identity_kernel<<<(d + 255) / 256, 256, 0, s>>>(g->X, d);
+    GQ_TRY(cudaGetLastError());
+    GQ_TRY(cudaEventRecord(g->ev_fork, s));
+    GQ_TRY(cudaStreamWaitEvent(g->side, g->ev_fork, 0));
     for (int k = 0; k < n; ++k) {
         gq_potrf_kernel<<<1, kPotrfThreads, kPotrfSmem, s>>>(g->F, d, k, g->Dinv, g->status);
         GQ_TRY(cudaGetLastError());
@@ -584,27 +766,26 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
         if (rem == 0) break;
         float* A21 = g->F + static_cast<size_t>(k + 1) * kNB * d + static_cast<size_t>(k) * kNB;
         float* A22 = g->F + static_cast<size_t>(k + 1) * kNB * (d + 1);
+        const float* Dk = g->Dinv + static_cast<size_t>(k) * kNB * kNB;
         // L21 = A21 inv(L11)^T, in place (one 128-wide column tile).
-        GQ_TRY(gemm<true>(A21, d, g->Dinv + static_cast<size_t>(k) * kNB * kNB, kNB, A21, d, rem, kNB, kNB,
-                          1.0f, 0, 0, s));
+        GQ_TRY(gemm<true>(A21, d, Dk, kNB, A21, d, rem, kNB, kNB, 1.0f, 0, 0, s));
+        GQ_TRY(cudaEventRecord(g->ev_panel, s));
         // A22 -= L21 L21^T on the tiles at or below the diagonal.
         GQ_TRY(gemm<true>(A21, d, A21, d, A22, d, rem, rem, kNB, -1.0f, 1, kGemmCLowerTiles, s));
+        // Side stream: M_k = L21 inv(L11), then B[k+1:, :k+1] -= M_k B_k.
+        GQ_TRY(cudaStreamWaitEvent(g->side, g->ev_panel, 0));
+        GQ_TRY(gemm<false>(A21, d, Dk, kNB, g->Mk, kNB, rem, kNB, kNB, 1.0f, 0, 0, g->side));
+        float* Bk = g->X + static_cast<size_t>(k) * kNB * d;
+        GQ_TRY(gemm<false>(g->Mk, kNB, Bk, d, Bk + static_cast<size_t>(kNB) * d, d, rem, (k + 1) * kNB, kNB, -1.0f,
+                           1, 0, g->side));
     }
-    // X = inv(L), block row by block row: X_k = inv(L_kk) (I_k - sum_{j<k} L_kj X_j),
-    // with the sum accumulated into X by rank-128 updates after each row.
-    GQ_TRY(cudaMemsetAsync(g->X, 0, dd * sizeof(float), s));
-    gq_identity_kernel<<<(d + 255) / 256, 256, 0, s>>>(g->X, d);
-    GQ_TRY(cudaGetLastError());
-    for (int k = 0; k < n; ++k) {
-        float* Xk = g->X + static_cast<size_t>(k) * kNB * d;
-        const int cols = (k + 1) * kNB;
-        GQ_TRY(gemm<false>(g->Dinv + static_cast<size_t>(k) * kNB * kNB, kNB, Xk, d, Xk, d, kNB, cols, kNB,
-                           1.0f, 0, 0, s));
-        const int rem = d - (k + 1) * kNB;
-        if (rem == 0) break;
-        const float* Lk = g->F + static_cast<size_t>(k + 1) * kNB * d + static_cast<size_t>(k) * kNB;
-        GQ_TRY(gemm<false>(Lk, d, Xk, d, Xk + static_cast<size_t>(kNB) * d, d, rem, cols, kNB, -1.0f, 1, 0, s));
-    }
+    GQ_TRY(cudaEventRecord(g->ev_side, g->side));
+    GQ_TRY(cudaStreamWaitEvent(s, g->ev_side, 0));
+    // X_k = inv(L_kk) B_k for every block row k, in place; tiles right of
+    // the diagonal block hold zeros and are skipped.
+    GQ_TRY(gemm<false>(g->Dinv, kNB, g->X, d, g->X, d, kNB, d, kNB, 1.0f, 0, kGemmCLowerTiles, s, n,
+                       static_cast<long long>(kNB) * kNB, static_cast<long long>(kNB) * d,
+                       static_cast<long long>(kNB) * d, kNB));
     // U = J X J into F.
     gq_reverse_copy_kernel<<<stride_grid(dd / 4, g->sm_count), 256, 0, s>>>(g->X, g->F, dd / 4);
     GQ_TRY(cudaGetLastError());
@@ -661,6 +842,11 @@ GQ_EXPORT hess_status gptq_create(int64_t d, int64_t max_rows, gptq_t* out) {
     if (e == cudaSuccess) e = cudaMalloc(&g->damp32, sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->loss, sizeof(double));
     if (e == cudaSuccess) e = cudaMalloc(&g->status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMalloc(&g->Mk, static_cast<size_t>(d) * kNB * sizeof(float));
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_panel, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_side, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         const hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
