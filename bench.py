@@ -590,6 +590,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-batches", type=int, default=2)
+    ap.add_argument("--quantize-only", action="store_true",
+                    help="run only the quantization-pass measurement and print its JSON")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -599,7 +601,10 @@ def main():
     else:
         from gptq_qqq_calibration_gb300 import build as b
         b.build()
-        run_ours(args)
+        if args.quantize_only:
+            print(json.dumps({"quantize_pass": _quantize_pass()}))
+        else:
+            run_ours(args)
 
 
 if __name__ == "__main__":

@@ -8,6 +8,7 @@
 // flush instead of once per batch (GPTQModel PR #2981, Changes: no transient
 // d x d product per batch; the accumulator is allocated once).
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -121,6 +122,11 @@ struct hess_ctx {
     double* damp64 = nullptr;
     float* damp32 = nullptr;
     cudaEvent_t ev = nullptr;
+    // The accumulator's last user: work on another stream waits for it
+    // (flushes may read-modify-write tiles without atomics).
+    cudaEvent_t ev_acc = nullptr;
+    cudaStream_t acc_stream = nullptr;
+    bool acc_used = false;
     int64_t N = 0;
     struct Pending {
         const void* ptr;
@@ -165,23 +171,43 @@ hess_status check_device(int dev) {
     return HESS_OK;
 }
 
-// Split-K factor: the fewest token slabs that keep >= 90 % of the grid busy
-// over all waves of (tile, slab) units.
+// Split-K factor (token slabs) from a per-unit cost model in SM cycles:
+// each unit costs max(MMA, epilogue), waves of units run back to back.  The
+// MMA part is ~300 cycles per 64-token k-block of a 128 x 128 tile; the
+// epilogue moves a 128 KB fp64 tile: ~12k cycles as a plain read-modify-
+// write (one slab, one writer per tile, HBM-bound) and ~36k with
+// red.add.f64 (several slabs; L2 applies fp64 adds at ~1.1 TB/s).  Small
+// flushes are epilogue-bound and take one slab; large ones split to fill
+// the waves.  Ties go to fewer slabs.
 int choose_slabs(int n_tiles, int total_kb, int grid) {
-    const int smax = std::max(1, std::min(64, total_kb / 2));
+    const int smax = std::max(1, std::min(64, total_kb));
     int best = 1;
-    double best_eff = 0.0;
+    double best_cost = 0.0;
     for (int S = 1; S <= smax; ++S) {
         const long long units = static_cast<long long>(n_tiles) * S;
         const long long waves = (units + grid - 1) / grid;
-        const double eff = static_cast<double>(units) / static_cast<double>(waves * grid);
-        if (eff >= 0.9) return S;
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
+        const double mma = 300.0 * std::ceil(static_cast<double>(total_kb) / S);
+        const double epi = S == 1 ? 12000.0 : 36000.0;
+        const double cost = static_cast<double>(waves) * std::max(mma, epi);
+        if (S == 1 || cost < best_cost * 0.98) {
+            best_cost = cost;
             best = S;
         }
     }
     return best;
+}
+
+// Order work on `s` after the accumulator's last user on another stream,
+// and record `s` as its user.
+hess_status order_acc(hess_ctx* h, cudaStream_t s) {
+    if (h->acc_used && h->acc_stream != s) CUDA_TRY(cudaStreamWaitEvent(s, h->ev_acc, 0));
+    return HESS_OK;
+}
+hess_status mark_acc(hess_ctx* h, cudaStream_t s) {
+    CUDA_TRY(cudaEventRecord(h->ev_acc, s));
+    h->acc_stream = s;
+    h->acc_used = true;
+    return HESS_OK;
 }
 
 hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
@@ -221,6 +247,10 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
                      : std::max(1, h->chunk_tokens / hk::kKBlock);
     p.d = static_cast<int32_t>(h->d);
     p.acc = h->acc;
+    {
+        hess_status st = order_acc(h, stream);
+        if (st != HESS_OK) return st;
+    }
     p.status = h->status;
     p.timeout_ns = h->timeout_ns;
     const bool pairs = !f32 && h->pair_kernel && h->max_pairs > 0;
@@ -232,6 +262,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(p.n_tiles, p.total_kb, pairs_max);
         p.n_units = p.n_tiles * p.n_slabs;
+        p.exclusive = p.n_slabs == 1 ? 1 : 0;
         grid = 2 * std::min(pairs_max, p.n_units);
         e = hk::launch_syrk_bf16_2sm(p, grid, stream);
     } else {
@@ -239,6 +270,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(h->n_tiles, p.total_kb, grid_max);
         p.n_units = p.n_tiles * p.n_slabs;
+        p.exclusive = p.n_slabs == 1 ? 1 : 0;
         grid = std::min(grid_max, p.n_units);
         e = f32 ? hk::launch_syrk_f32(p, grid, stream) : hk::launch_syrk_bf16(p, grid, stream);
     }
@@ -246,9 +278,13 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     h->pending_tokens = 0;
     h->pending_dtype = -1;
     if (e != cudaSuccess) return fail(HESS_ERR_CUDA, "SYRK launch failed: %s", cudaGetErrorString(e));
+    {
+        hess_status st = mark_acc(h, stream);
+        if (st != HESS_OK) return st;
+    }
     if (std::getenv("HESS_TRACE"))
-        std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d grid=%d %s (max pairs %d)\n",
-                     static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, grid,
+        std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d%s grid=%d %s (max pairs %d)\n",
+                     static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, p.exclusive ? " (exclusive)" : "", grid,
                      f32 ? "f32" : (pairs ? "bf16-pairs" : "bf16"), h->max_pairs);
     return HESS_OK;
 }
@@ -298,6 +334,7 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     if (e == cudaSuccess) e = cudaMemset(h->acc, 0, acc_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_acc, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
@@ -306,6 +343,7 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
         cudaFree(h->damp64);
         cudaFree(h->damp32);
         if (h->ev) cudaEventDestroy(h->ev);
+        if (h->ev_acc) cudaEventDestroy(h->ev_acc);
         delete h->params;
         delete h;
         return fail(s, "hess_create: %s", cudaGetErrorString(e));
@@ -376,9 +414,11 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
         return HESS_OK;
     }
     const double scale = 2.0 / static_cast<double>(h->N);
+    if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(hk::launch_diag_damp(h->acc, static_cast<int>(h->d), h->T, scale, damp_percent,
                                   h->damp64, h->damp32, s));
     CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, h->damp64, s));
+    if ((st = mark_acc(h, s)) != HESS_OK) return st;
     if (damp_value_out) {
         float v = 0.0f;
         CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
@@ -421,10 +461,11 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->pending_tokens = 0;
     h->pending_dtype = -1;
     h->N = 0;
+    if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemsetAsync(h->acc, 0,
                              static_cast<size_t>(h->n_tiles) * hk::kTileElems * sizeof(double), s));
     CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
-    return HESS_OK;
+    return mark_acc(h, s);
 }
 
 HESS_EXPORT hess_status hess_set_option(hess_t h, int32_t option, int64_t value) {
@@ -479,6 +520,7 @@ HESS_EXPORT hess_status hess_destroy(hess_t h) {
         cudaFree(h->damp64);
         cudaFree(h->damp32);
         cudaEventDestroy(h->ev);
+        cudaEventDestroy(h->ev_acc);
         cudaSetDevice(cur);
     }
     delete h->params;
@@ -506,7 +548,9 @@ HESS_EXPORT hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream)
     if ((st = flush_locked(src, s)) != HESS_OK) return st;
     if ((st = flush_locked(dst, s)) != HESS_OK) return st;
     const size_t n = static_cast<size_t>(dst->n_tiles) * hk::kTileElems;
+    if ((st = order_acc(src, s)) != HESS_OK || (st = order_acc(dst, s)) != HESS_OK) return st;
     CUDA_TRY(hk::launch_add_f64(dst->acc, src->acc, n, dst->sm_count, s));
+    if ((st = mark_acc(src, s)) != HESS_OK || (st = mark_acc(dst, s)) != HESS_OK) return st;
     dst->N += src->N;
     return HESS_OK;
 }
@@ -528,11 +572,19 @@ HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream
     std::lock_guard<std::mutex> lk(src->mu);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t bytes = static_cast<size_t>(src->n_tiles) * hk::kTileElems * sizeof(double);
+    if ((st = order_acc(src, s)) != HESS_OK) {
+        hess_destroy(h);
+        return st;
+    }
     cudaError_t e = cudaMemcpyAsync(h->acc, src->acc, bytes, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaEventRecord(src->ev_acc, s);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_acc, s);
     if (e != cudaSuccess) {
         hess_destroy(h);
         return fail(HESS_ERR_CUDA, "clone copy failed: %s", cudaGetErrorString(e));
     }
+    src->acc_stream = h->acc_stream = s;
+    src->acc_used = h->acc_used = true;
     h->N = src->N;
     h->flush_tokens = src->flush_tokens;
     h->max_pending = src->max_pending;

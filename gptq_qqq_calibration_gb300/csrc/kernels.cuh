@@ -47,6 +47,8 @@ struct SyrkParams {
     int32_t chunk_kb;       // k-blocks per tensor-memory accumulation chain
     int32_t d;
     int32_t n_units;        // n_tiles * n_slabs
+    int32_t exclusive;      // 1: one token slab, so each accumulator tile has one writer and the
+                            // epilogue reads, adds and stores it (else red.add.f64)
     double* acc;            // fp64 accumulator (tile layout above)
     uint32_t* status;
     unsigned long long timeout_ns;

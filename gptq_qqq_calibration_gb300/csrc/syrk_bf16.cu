@@ -50,6 +50,7 @@ constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 128, 128);
 constexpr int kNumBarriers = 2 * kStages + 5;
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + 8 * kNumBarriers + 16;
 
+template <bool kExcl>
 __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_constant__ SyrkParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
-        syrk::epilogue(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+        syrk::epilogue<kExcl>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
     }
 
     tc_fence_before();
@@ -212,12 +213,18 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
 size_t syrk_bf16_smem_bytes() { return kSmemBytes; }
 
 cudaError_t syrk_bf16_prepare() {
-    return cudaFuncSetAttribute(syrk_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(syrk_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(syrk_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemBytes));
 }
 
 cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s) {
-    syrk_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    if (p.exclusive)
+        syrk_bf16_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+    else
+        syrk_bf16_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 

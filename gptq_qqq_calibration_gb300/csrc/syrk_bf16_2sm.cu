@@ -69,6 +69,7 @@ __device__ __forceinline__ bool pair_unit_at(const SyrkParams& p, int u, PairUni
     return un.k1 > un.k0;
 }
 
+template <bool kExcl>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     syrk_bf16_2sm_kernel(const __grid_constant__ SyrkParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -214,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue (8 warps)
         const int T = p.tiles_per_dim;
         const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-        syrk::epilogue_t(
+        syrk::epilogue_t<kExcl>(
             p, tmem, warp, lane, 2, accf_bar(0), pair, n_pairs,
             [&](int u, int& k0, int& k1, int& out_tile) {
                 PairUnit un;
@@ -251,9 +252,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 size_t syrk_bf16_2sm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
-    cudaError_t e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel,
+    cudaError_t e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     int dev = 0, sms = 0;
@@ -263,7 +267,7 @@ cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, syrk_bf16_2sm_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, syrk_bf16_2sm_kernel<false>, &cfg);
     if (e != cudaSuccess || clusters <= 0) {
         cudaGetLastError();
         clusters = sms / 2;
@@ -273,7 +277,10 @@ cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
 }
 
 cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s) {
-    syrk_bf16_2sm_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    if (p.exclusive)
+        syrk_bf16_2sm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+    else
+        syrk_bf16_2sm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 

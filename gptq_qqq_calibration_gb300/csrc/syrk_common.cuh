@@ -41,11 +41,13 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 // (warp % 4) and kEpiCols of the 128 columns, adds the two banks, and folds the
 // sum into a (hi, lo) pair with Fast2Sum on packed fp32 pairs.  At the
 // end of a unit, hi + lo is added in fp64 to accumulator tile `out_tile`
-// (skipped when it is negative).
+// (skipped when it is negative): by red.add.f64, or by a plain
+// read-modify-write when the launch has one token slab (kExcl, the kernel
+// instance chosen when p.exclusive is set).
 //   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
 //   wait_full(bar, parity) waits for a filled accumulator buffer;
 //   arrive_empty(b) releases buffer b to the MMA issuer.
-template <class UnitFn, class WaitFn, class ArriveFn>
+template <bool kExcl, class UnitFn, class WaitFn, class ArriveFn>
 __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, int warp, int lane,
                                            int first_warp, uint32_t accf_bar0, int u0, int ustride,
                                            UnitFn unit_fn, WaitFn wait_full, ArriveFn arrive_empty) {
@@ -103,23 +105,45 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         if (out_tile < 0) continue;
         double* const out = p.acc + static_cast<size_t>(out_tile) * kTileElems +
                             static_cast<size_t>(col0) * kTile + row;
+        if constexpr (kExcl) {
+            // Sole writer of this tile in this launch: a plain read-modify-
+            // write, eight columns' loads in flight at a time.
 #pragma unroll
-        for (int i = 0; i < kEpiCols / 2; ++i) {
-            float h0, h1, l0, l1;
-            unpack2(hi[i], h0, h1);
-            unpack2(lo[i], l0, l1);
-            red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
-            red_add_f64(out + (2 * i + 1) * kTile, static_cast<double>(h1) + static_cast<double>(l1));
+            for (int g = 0; g < kEpiCols / 8; ++g) {
+                double old[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) old[i] = out[(8 * g + i) * kTile];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float h0, h1, l0, l1;
+                    unpack2(hi[4 * g + i], h0, h1);
+                    unpack2(lo[4 * g + i], l0, l1);
+                    out[(8 * g + 2 * i) * kTile] =
+                        old[2 * i] + (static_cast<double>(h0) + static_cast<double>(l0));
+                    out[(8 * g + 2 * i + 1) * kTile] =
+                        old[2 * i + 1] + (static_cast<double>(h1) + static_cast<double>(l1));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kEpiCols / 2; ++i) {
+                float h0, h1, l0, l1;
+                unpack2(hi[i], h0, h1);
+                unpack2(lo[i], l0, l1);
+                red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
+                red_add_f64(out + (2 * i + 1) * kTile, static_cast<double>(h1) + static_cast<double>(l1));
+            }
         }
     }
     if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);
 }
 
 // The single-CTA form: units in blockIdx.x + k * gridDim.x order, local barriers.
+template <bool kExcl>
 __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int warp, int lane,
                                          int first_warp, uint32_t accf_bar0, uint32_t acce_bar0,
                                          unsigned long long limit) {
-    epilogue_t(
+    epilogue_t<kExcl>(
         p, tmem, warp, lane, first_warp, accf_bar0, blockIdx.x, gridDim.x,
         [&](int u, int& k0, int& k1, int& out_tile) {
             Unit un;

@@ -92,6 +92,7 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
     lo = __fsub_rn(x, hi);
 }
 
+template <bool kExcl>
 __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_constant__ SyrkParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
-        syrk::epilogue(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+        syrk::epilogue<kExcl>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
     }
 
     tc_fence_before();
@@ -292,12 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
 size_t syrk_f32_smem_bytes() { return kSmemBytes; }
 
 cudaError_t syrk_f32_prepare() {
-    return cudaFuncSetAttribute(syrk_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(syrk_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(syrk_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemBytes));
 }
 
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s) {
-    syrk_f32_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    if (p.exclusive)
+        syrk_f32_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+    else
+        syrk_f32_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
