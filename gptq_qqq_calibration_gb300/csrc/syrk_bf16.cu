@@ -216,8 +216,14 @@ cudaError_t syrk_bf16_prepare() {
     cudaError_t e = cudaFuncSetAttribute(syrk_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(syrk_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes));
+    e = cudaFuncSetAttribute(syrk_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    // One CTA of kThreads must fit an SM with this register and shared-memory use.
+    int blocks = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, syrk_bf16_kernel<false>, kThreads, kSmemBytes);
+    if (e == cudaSuccess && blocks < 1) e = cudaErrorLaunchOutOfResources;
+    return e;
 }
 
 cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s) {

@@ -296,8 +296,14 @@ cudaError_t syrk_f32_prepare() {
     cudaError_t e = cudaFuncSetAttribute(syrk_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(syrk_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes));
+    e = cudaFuncSetAttribute(syrk_f32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    // One CTA of kThreads must fit an SM with this register and shared-memory use.
+    int blocks = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, syrk_f32_kernel<false>, kThreads, kSmemBytes);
+    if (e == cudaSuccess && blocks < 1) e = cudaErrorLaunchOutOfResources;
+    return e;
 }
 
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s) {
