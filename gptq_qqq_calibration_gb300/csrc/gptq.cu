@@ -131,6 +131,68 @@ constexpr size_t kPotrfFloats =
     2 * kNB * kLd + kSub * kLtLd + kSub * kYtLd + kNB;
 constexpr size_t kPotrfSmem = kPotrfFloats * sizeof(float);
 
+// Step 1 of the diagonal-block kernel for the sub-panel at column P, run by
+// one warp: register factor of the kSub x kSub diagonal sub-block and its
+// inverse (into S, Xs's diagonal sub-block, Yt and rl).  Returns true if a
+// pivot was replaced.  Inlined at both call sites: as a call it cost the
+// critical warp more than the duplicated code costs the instruction cache.
+__device__ __forceinline__ bool potrf_sub_block(float* S, float* Xs, float* Yt, float* rl, int P, int lane) {
+    bool bad = false;
+    // Lanes kSub..31 take part in the shuffles only.
+    const bool in = lane < kSub;
+    float dv[kSub];
+#pragma unroll
+    for (int c = 0; c < kSub; ++c) dv[c] = in ? S[(P + lane) * kLd + P + c] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) {
+        float piv = __shfl_sync(kFull, dv[j], j);
+        if (!(piv > 0.0f) || !(piv < INFINITY)) {
+            bad = true;
+            piv = 1.0f;
+        }
+        // 1/sqrt by the hardware estimate and one Newton step,
+        // y <- y (1.5 - 0.5 x y^2): the pivot chain is the
+        // sequential path of the whole factorization.
+        float il = rsqrtf(piv);
+        il = __fmul_rn(il, fmaf(-0.5f * piv * il, il, 1.5f));
+        const float l = __fmul_rn(piv, il);
+        if (lane == j) dv[j] = l;
+        else if (lane > j) dv[j] = __fmul_rn(dv[j], il);
+        if (lane == 0) rl[P + j] = il;
+#pragma unroll
+        for (int c = 0; c < kSub; ++c) {
+            if (c > j) {  // resolved at compile time
+                const float lc = __shfl_sync(kFull, dv[j], c);
+                if (lane >= c) dv[c] = fmaf(-dv[j], lc, dv[c]);
+            }
+        }
+    }
+    if (in) {
+#pragma unroll
+        for (int c = 0; c < kSub; ++c) S[(P + lane) * kLd + P + c] = c <= lane ? dv[c] : 0.0f;
+    }
+    __syncwarp();
+    // Column `lane` of the sub-block inverse: solve L y = e_lane.
+    float acc[kSub];
+#pragma unroll
+    for (int i = 0; i < kSub; ++i) acc[i] = i == lane ? 1.0f : 0.0f;
+#pragma unroll
+    for (int m = 0; m < kSub; ++m) {
+        acc[m] = __fmul_rn(acc[m], rl[P + m]);
+#pragma unroll
+        for (int i = 0; i < kSub; ++i)
+            if (i > m) acc[i] = fmaf(-S[(P + i) * kLd + P + m], acc[m], acc[i]);
+    }
+    if (in) {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+            Xs[(P + i) * kLd + P + lane] = acc[i];  // Y[i][lane] (0 for i < lane)
+            Yt[lane * kYtLd + i] = acc[i];           // Yt[m][c] = Y[c][m]
+        }
+    }
+    return bad;
+}
+
 __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __restrict__ F, int d, int k,
                                                                  float* __restrict__ Dinv,
                                                                  int* __restrict__ status) {
@@ -165,59 +227,8 @@ __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __res
     bool bad = false;
     for (int p = 0; p < kNB / kSub; ++p) {
         const int P = p * kSub;
-        if (warp == 0) {
-            // Lanes kSub..31 take part in the shuffles only.
-            const bool in = lane < kSub;
-            float dv[kSub];
-#pragma unroll
-            for (int c = 0; c < kSub; ++c) dv[c] = in ? S[(P + lane) * kLd + P + c] : 0.0f;
-#pragma unroll
-            for (int j = 0; j < kSub; ++j) {
-                float piv = __shfl_sync(kFull, dv[j], j);
-                if (!(piv > 0.0f) || !(piv < INFINITY)) {
-                    bad = true;
-                    piv = 1.0f;
-                }
-                // 1/sqrt by the hardware estimate and one Newton step,
-                // y <- y (1.5 - 0.5 x y^2): the pivot chain is the
-                // sequential path of the whole factorization.
-                float il = rsqrtf(piv);
-                il = __fmul_rn(il, fmaf(-0.5f * piv * il, il, 1.5f));
-                const float l = __fmul_rn(piv, il);
-                if (lane == j) dv[j] = l;
-                else if (lane > j) dv[j] = __fmul_rn(dv[j], il);
-                if (lane == 0) rl[P + j] = il;
-#pragma unroll
-                for (int c = 0; c < kSub; ++c) {
-                    if (c > j) {  // resolved at compile time
-                        const float lc = __shfl_sync(kFull, dv[j], c);
-                        if (lane >= c) dv[c] = fmaf(-dv[j], lc, dv[c]);
-                    }
-                }
-            }
-            if (in) {
-#pragma unroll
-                for (int c = 0; c < kSub; ++c) S[(P + lane) * kLd + P + c] = c <= lane ? dv[c] : 0.0f;
-            }
-            __syncwarp();
-            // Column `lane` of the sub-block inverse: solve L y = e_lane.
-            float acc[kSub];
-#pragma unroll
-            for (int i = 0; i < kSub; ++i) acc[i] = i == lane ? 1.0f : 0.0f;
-#pragma unroll
-            for (int m = 0; m < kSub; ++m) {
-                acc[m] = __fmul_rn(acc[m], rl[P + m]);
-#pragma unroll
-                for (int i = 0; i < kSub; ++i)
-                    if (i > m) acc[i] = fmaf(-S[(P + i) * kLd + P + m], acc[m], acc[i]);
-            }
-            if (in) {
-#pragma unroll
-                for (int i = 0; i < kSub; ++i) {
-                    Xs[(P + i) * kLd + P + lane] = acc[i];  // Y[i][lane] (0 for i < lane)
-                    Yt[lane * kYtLd + i] = acc[i];           // Yt[m][c] = Y[c][m]
-                }
-            }
+        if (p == 0) {  // later sub-panels are factored inside step 3 of the previous one
+            if (warp == 0) bad |= potrf_sub_block(S, Xs, Yt, rl, P, lane);
         }
         __syncthreads();
         const int R0 = P + kSub;  // first row after the sub-panel
@@ -282,12 +293,17 @@ __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __res
         __syncthreads();
         if (nb == 0) break;
         // 3. On 4 x 4 tiles: A22 -= L21 L21^T at or below the diagonal
-        //    (idx < n3), and B_i,j -= L_ip X_p,j for the rows after the
-        //    sub-panel and the columns up to its end (the rest).
+        //    (triangular index idx < n3), and B_i,j -= L_ip X_p,j for the rows
+        //    after the sub-panel and the columns up to its end (the rest).
+        //    Look-ahead: warp 0 updates the next diagonal sub-block (the
+        //    first kSubT (kSubT + 1) / 2 tiles) and factors it at once, while
+        //    the other warps apply the rest of the update; the next
+        //    sub-panel's factor touches none of their tiles.
         const int nt = nb / 4;
         const int n3 = nt * (nt + 1) / 2;
         const int ct = (P + kSub) / 4;
-        for (int idx = tid; idx < n3 + nt * ct; idx += kPotrfThreads) {
+        constexpr int kDiagTiles = kSubT * (kSubT + 1) / 2;
+        auto tile = [&](int idx) {
             float a3[4][4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
@@ -331,6 +347,13 @@ __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __res
 #pragma unroll
                     for (int u = 0; u < 4; ++u) Xs[(R0 + 4 * ta + t) * kLd + 4 * tb + u] -= a3[t][u];
             }
+        };
+        if (warp == 0) {
+            if (lane < kDiagTiles) tile(lane);
+            __syncwarp();
+            bad |= potrf_sub_block(S, Xs, Yt, rl, R0, lane);
+        } else {
+            for (int idx = kDiagTiles + tid - 32; idx < n3 + nt * ct; idx += kPotrfThreads - 32) tile(idx);
         }
         __syncthreads();
     }
@@ -364,29 +387,33 @@ struct GemmArgs {
 };
 
 // C = beta C + alpha A op(B) in fp32 (FMA chains along k, one rounding per
-// step).  128 x 128 output tile per CTA, k-slices of 8 double-buffered in
-// shared memory, 8 x 8 outputs per thread.  N % 128 == 0 and K % 8 == 0;
-// rows of A and C beyond M are skipped.  A CTA reads only the rows of A and
-// the columns of op(B) of its own tile, and writes C after all its reads,
-// so C may alias A when N == 128, or alias B when K == 128 and op(B) is not
-// transposed.
-template <bool kTransB>
+// step).  BM x 128 output tile per CTA (BM = 128, or 32 for narrow problems
+// whose 128-row grid would not fill the SMs), k-slices of 8 double-buffered
+// in shared memory, BM/16 x 8 outputs per thread.  N % 128 == 0 and
+// K % 8 == 0; rows of A and C beyond M are skipped.  A CTA reads only the
+// rows of A and the columns of op(B) of its own tile, and writes C after all
+// its reads, so C may alias A when N == 128, or alias B when K == 128, op(B)
+// is not transposed and one row tile covers M (BM = 128 >= M).
+template <bool kTransB, int BM>
 __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
-    const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
-    if ((g.flags & kGemmCLowerTiles) && n0 > m0 + static_cast<int>(blockIdx.z) * g.diag_step) return;
+    static_assert(BM == 128 || BM == 32, "tile height");
+    constexpr int RM = BM / 16;  // rows per thread
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * 128;
+    if ((g.flags & kGemmCLowerTiles) && n0 >= m0 + BM + static_cast<int>(blockIdx.z) * g.diag_step) return;
     const float* Ab = g.A + blockIdx.z * g.sA;
     const float* Bb = g.B + blockIdx.z * g.sB;
     float* Cb = g.C + blockIdx.z * g.sC;
-    __shared__ __align__(16) float As[2][8][kGemmLd];
+    __shared__ __align__(16) float As[2][8][BM + 4];
     __shared__ __align__(16) float Bs[2][8][kGemmLd];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int r_row = tid >> 1, r_col = (tid & 1) * 4;      // row-of-8 loader (A, transposed B)
-    const int b_k = tid >> 5, b_n = (tid & 31) * 4;         // plain B loader
-    const bool a_ok = m0 + r_row < g.M;
+    const int r_row = tid >> 1, r_col = (tid & 1) * 4;  // row-of-8 loader (A, transposed B)
+    const int b_k = tid >> 5, b_n = (tid & 31) * 4;     // plain B loader
+    const bool a_loader = r_row < BM;
+    const bool a_ok = a_loader && m0 + r_row < g.M;
     const float* a_src = Ab + static_cast<size_t>(a_ok ? m0 + r_row : 0) * g.lda + r_col;
-    float acc[8][8];
+    float acc[RM][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RM; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
@@ -400,10 +427,12 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
             rb = *reinterpret_cast<const float4*>(Bb + static_cast<size_t>(k0 + b_k) * g.ldb + n0 + b_n);
     };
     auto store = [&](int buf) {
-        As[buf][r_col + 0][r_row] = ra.x;
-        As[buf][r_col + 1][r_row] = ra.y;
-        As[buf][r_col + 2][r_row] = ra.z;
-        As[buf][r_col + 3][r_row] = ra.w;
+        if (a_loader) {
+            As[buf][r_col + 0][r_row] = ra.x;
+            As[buf][r_col + 1][r_row] = ra.y;
+            As[buf][r_col + 2][r_row] = ra.z;
+            As[buf][r_col + 3][r_row] = ra.w;
+        }
         if (kTransB) {
             Bs[buf][r_col + 0][r_row] = rb.x;
             Bs[buf][r_col + 1][r_row] = rb.y;
@@ -413,6 +442,8 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
             *reinterpret_cast<float4*>(&Bs[buf][b_k][b_n]) = rb;
         }
     };
+    // the row of thread row i within the tile
+    auto row_of = [&](int i) { return BM == 128 ? (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4) : ty * RM + i; };
 
     load(0);
     store(0);
@@ -423,14 +454,21 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
         if (more) load(k0 + 8);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+            float a[RM];
+            if constexpr (BM == 128) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+                a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+                a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+            } else {
+                const float2 a0 = *reinterpret_cast<const float2*>(&As[buf][kk][ty * RM]);
+                a[0] = a0.x; a[1] = a0.y;
+            }
             const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
             const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < RM; ++i)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
@@ -440,8 +478,8 @@ __global__ void __launch_bounds__(256) gq_gemm_kernel(const GemmArgs g) {
     }
 
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    for (int i = 0; i < RM; ++i) {
+        const int m = m0 + row_of(i);
         if (m >= g.M) continue;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -661,14 +699,22 @@ hess_status gq_fail(hess_status s, const char* fmt, ...) {
             return gq_fail(HESS_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));     \
     } while (0)
 
+// `narrow_ok`: 32-row tiles may be used (not when C aliases B, whose
+// column tile would then be shared by several CTAs).
 template <bool kTransB>
-cudaError_t gemm(const float* A, int lda, const float* B, int ldb, float* C, int ldc, int M, int N, int K,
-                 float alpha, int beta, int flags, cudaStream_t s, int batch = 1, long long sA = 0,
-                 long long sB = 0, long long sC = 0, int diag_step = 0) {
+cudaError_t gemm(int sm_count, const float* A, int lda, const float* B, int ldb, float* C, int ldc, int M,
+                 int N, int K, float alpha, int beta, int flags, cudaStream_t s, int batch = 1,
+                 long long sA = 0, long long sB = 0, long long sC = 0, int diag_step = 0,
+                 bool narrow_ok = true) {
     if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return cudaSuccess;
     GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, alpha, beta, flags, sA, sB, sC, diag_step};
-    const dim3 grid(N / 128, (M + 127) / 128, batch);
-    gq_gemm_kernel<kTransB><<<grid, 256, 0, s>>>(g);
+    // 128-row tiles unless they leave SMs idle; then 32-row tiles (4x the CTAs).
+    const long long tiles128 = static_cast<long long>(N / 128) * ((M + 127) / 128) * batch;
+    if (tiles128 >= sm_count || !narrow_ok) {
+        gq_gemm_kernel<kTransB, 128><<<dim3(N / 128, (M + 127) / 128, batch), 256, 0, s>>>(g);
+    } else {
+        gq_gemm_kernel<kTransB, 32><<<dim3(N / 128, (M + 31) / 32, batch), 256, 0, s>>>(g);
+    }
     return cudaGetLastError();
 }
 
@@ -768,24 +814,24 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
         float* A22 = g->F + static_cast<size_t>(k + 1) * kNB * (d + 1);
         const float* Dk = g->Dinv + static_cast<size_t>(k) * kNB * kNB;
         // L21 = A21 inv(L11)^T, in place (one 128-wide column tile).
-        GQ_TRY(gemm<true>(A21, d, Dk, kNB, A21, d, rem, kNB, kNB, 1.0f, 0, 0, s));
+        GQ_TRY(gemm<true>(g->sm_count, A21, d, Dk, kNB, A21, d, rem, kNB, kNB, 1.0f, 0, 0, s));
         GQ_TRY(cudaEventRecord(g->ev_panel, s));
         // A22 -= L21 L21^T on the tiles at or below the diagonal.
-        GQ_TRY(gemm<true>(A21, d, A21, d, A22, d, rem, rem, kNB, -1.0f, 1, kGemmCLowerTiles, s));
+        GQ_TRY(gemm<true>(g->sm_count, A21, d, A21, d, A22, d, rem, rem, kNB, -1.0f, 1, kGemmCLowerTiles, s));
         // Side stream: M_k = L21 inv(L11), then B[k+1:, :k+1] -= M_k B_k.
         GQ_TRY(cudaStreamWaitEvent(g->side, g->ev_panel, 0));
-        GQ_TRY(gemm<false>(A21, d, Dk, kNB, g->Mk, kNB, rem, kNB, kNB, 1.0f, 0, 0, g->side));
+        GQ_TRY(gemm<false>(g->sm_count, A21, d, Dk, kNB, g->Mk, kNB, rem, kNB, kNB, 1.0f, 0, 0, g->side));
         float* Bk = g->X + static_cast<size_t>(k) * kNB * d;
-        GQ_TRY(gemm<false>(g->Mk, kNB, Bk, d, Bk + static_cast<size_t>(kNB) * d, d, rem, (k + 1) * kNB, kNB, -1.0f,
+        GQ_TRY(gemm<false>(g->sm_count, g->Mk, kNB, Bk, d, Bk + static_cast<size_t>(kNB) * d, d, rem, (k + 1) * kNB, kNB, -1.0f,
                            1, 0, g->side));
     }
     GQ_TRY(cudaEventRecord(g->ev_side, g->side));
     GQ_TRY(cudaStreamWaitEvent(s, g->ev_side, 0));
     // X_k = inv(L_kk) B_k for every block row k, in place; tiles right of
     // the diagonal block hold zeros and are skipped.
-    GQ_TRY(gemm<false>(g->Dinv, kNB, g->X, d, g->X, d, kNB, d, kNB, 1.0f, 0, kGemmCLowerTiles, s, n,
+    GQ_TRY(gemm<false>(g->sm_count, g->Dinv, kNB, g->X, d, g->X, d, kNB, d, kNB, 1.0f, 0, kGemmCLowerTiles, s, n,
                        static_cast<long long>(kNB) * kNB, static_cast<long long>(kNB) * d,
-                       static_cast<long long>(kNB) * d, kNB));
+                       static_cast<long long>(kNB) * d, kNB, /*narrow_ok=*/false));
     // U = J X J into F.
     gq_reverse_copy_kernel<<<stride_grid(dd / 4, g->sm_count), 256, 0, s>>>(g->X, g->F, dd / 4);
     GQ_TRY(cudaGetLastError());
@@ -960,13 +1006,13 @@ GQ_EXPORT hess_status gptq_quantize(gptq_t g, const void* W, int32_t w_dtype, in
                 GQ_TRY(cudaGetLastError());
                 const int in_super = (sb1 - b - 1) * kNB;  // columns left in this super-block
                 if (in_super > 0)
-                    GQ_TRY(gemm<false>(err_b, ld_err, g->F + static_cast<size_t>(b) * kNB * d + (b + 1) * kNB, d,
+                    GQ_TRY(gemm<false>(g->sm_count, err_b, ld_err, g->F + static_cast<size_t>(b) * kNB * d + (b + 1) * kNB, d,
                                        g->Wc + (b + 1) * kNB, d, static_cast<int>(rows), in_super, kNB, -1.0f, 1, 0,
                                        s));
             }
             const int rest = d - sb1 * kNB;
             if (rest > 0)
-                GQ_TRY(gemm<false>(g->Err, ld_err, g->F + static_cast<size_t>(sb0) * kNB * d + sb1 * kNB, d,
+                GQ_TRY(gemm<false>(g->sm_count, g->Err, ld_err, g->F + static_cast<size_t>(sb0) * kNB * d + sb1 * kNB, d,
                                    g->Wc + sb1 * kNB, d, static_cast<int>(rows), rest, (sb1 - sb0) * kNB, -1.0f, 1,
                                    0, s));
         }

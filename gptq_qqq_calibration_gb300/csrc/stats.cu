@@ -4,6 +4,8 @@
 //   * the imatrix per-column sum of squares, which NVIDIA Model-Optimizer
 //     PR #3002 ("What does this PR do?") keeps as a float32 statistic because
 //     it is not a GEMM.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
@@ -17,13 +19,13 @@ __global__ void __launch_bounds__(256) add_f64_kernel(double* __restrict__ dst,
     const size_t n4 = n / 4;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
-        double4 a = reinterpret_cast<double4*>(dst)[i];
-        const double4 b = reinterpret_cast<const double4*>(src)[i];
+        double4_32a a = reinterpret_cast<double4_32a*>(dst)[i];
+        const double4_32a b = reinterpret_cast<const double4_32a*>(src)[i];
         a.x += b.x;
         a.y += b.y;
         a.z += b.z;
         a.w += b.w;
-        reinterpret_cast<double4*>(dst)[i] = a;
+        reinterpret_cast<double4_32a*>(dst)[i] = a;
     }
     for (size_t i = n4 * 4 + blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
          i += stride)
@@ -54,40 +56,58 @@ __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// Thread = 8 consecutive features of one token slab.  Squares are summed in
-// fp32 chains of kChain tokens (round to nearest: unbiased), each chain is
-// folded into a compensated (hi, lo) pair, and the slab's total is added in
-// fp64 to acc.  Each warp reads 32 x 16 contiguous bytes of a token row.
+// CTA = 256 consecutive features x one token slab; warp w takes the slab's
+// tokens w, w + 8, w + 16, ..., and lane l features 8l..8l+7 of the group, so
+// each warp reads 512 contiguous bytes of a token row (bf16).  Squares are
+// summed in fp32 chains of kChain tokens (round to nearest: unbiased), each
+// chain folded into a compensated (hi, lo) pair; the eight warps' totals are
+// added in fp64 through shared memory and the CTA adds one fp64 value per
+// feature to acc.  One atomic per feature per CTA keeps the L2 fp64 adds
+// (about 1.1 TB/s) far below the bytes streamed.
 constexpr int kChain = 64;
+constexpr int kColWarps = 8;
+constexpr int kColFeatures = 256;  // features per CTA (32 lanes x 8)
 
 template <class T>
-__global__ void __launch_bounds__(256) colsumsq_kernel(const T* __restrict__ X, int64_t n, int d,
-                                                       int64_t slab, double* __restrict__ acc) {
-    const int f0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-    if (f0 >= d) return;
+__global__ void __launch_bounds__(kColWarps * 32) colsumsq_kernel(const T* __restrict__ X, int64_t n, int d,
+                                                                  int64_t slab, double* __restrict__ acc) {
+    __shared__ double part[kColWarps][kColFeatures];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int f0 = blockIdx.x * kColFeatures + lane * 8;
+    const bool active = f0 < d;
     const int64_t t0 = static_cast<int64_t>(blockIdx.y) * slab;
     const int64_t t1 = min(n, t0 + slab);
     float hi[8] = {}, lo[8] = {};
-    for (int64_t c0 = t0; c0 < t1; c0 += kChain) {
-        const int64_t c1 = min(t1, c0 + kChain);
-        float s[8] = {};
+    if (active) {
+        for (int64_t c0 = t0 + warp; c0 < t1; c0 += static_cast<int64_t>(kColWarps) * kChain) {
+            const int64_t c1 = min(t1, c0 + static_cast<int64_t>(kColWarps) * kChain);
+            float s[8] = {};
 #pragma unroll 8
-        for (int64_t t = c0; t < c1; ++t) {
-            float x[8];
-            load8(X + t * d + f0, x);
+            for (int64_t t = c0; t < c1; t += kColWarps) {
+                float x[8];
+                load8(X + t * d + f0, x);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[k], x[k], s[k]);
-        }
+                for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[k], x[k], s[k]);
+            }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float e;
-            hi[k] = two_sum(hi[k], s[k], e);
-            lo[k] = __fadd_rn(lo[k], e);
+            for (int k = 0; k < 8; ++k) {
+                float e;
+                hi[k] = two_sum(hi[k], s[k], e);
+                lo[k] = __fadd_rn(lo[k], e);
+            }
         }
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        atomicAdd(acc + f0 + k, static_cast<double>(hi[k]) + static_cast<double>(lo[k]));
+        part[warp][lane * 8 + k] = static_cast<double>(hi[k]) + static_cast<double>(lo[k]);
+    __syncthreads();
+    const int f = blockIdx.x * kColFeatures + threadIdx.x;
+    if (f < d) {
+        double t = 0.0;
+#pragma unroll
+        for (int w = 0; w < kColWarps; ++w) t += part[w][threadIdx.x];
+        if (t != 0.0) atomicAdd(acc + f, t);
+    }
 }
 
 __global__ void __launch_bounds__(256) colsumsq_read_kernel(const double* __restrict__ acc,
@@ -107,22 +127,25 @@ cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_coun
 
 cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
                             cudaStream_t s) {
-    const int gx = (d / 8 + 255) / 256;
-    // enough token slabs for about 8 CTAs per SM, at least one chain each
+    const int gx = (d + kColFeatures - 1) / kColFeatures;
+    // token slabs: multiples of one chain per warp, enough of them for about
+    // 8 CTAs per SM
+    const int64_t unit = static_cast<int64_t>(kColWarps) * kChain;
     int64_t slabs = (8LL * sm_count + gx - 1) / gx;
     int64_t slab = (n + slabs - 1) / slabs;
-    slab = ((slab + kChain - 1) / kChain) * kChain;
+    slab = std::max<int64_t>(unit, ((slab + unit - 1) / unit) * unit);
     slabs = (n + slab - 1) / slab;
     if (slabs > 65535) {
         slabs = 65535;
-        slab = (n + slabs - 1) / slabs;
+        slab = (((n + slabs - 1) / slabs + unit - 1) / unit) * unit;
+        slabs = (n + slab - 1) / slab;
     }
     const dim3 grid(gx, static_cast<unsigned>(slabs));
     if (f32)
-        colsumsq_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), n, d, slab, acc);
+        colsumsq_kernel<float><<<grid, kColWarps * 32, 0, s>>>(static_cast<const float*>(X), n, d, slab, acc);
     else
         colsumsq_kernel<__nv_bfloat16>
-            <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n, d, slab, acc);
+            <<<grid, kColWarps * 32, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n, d, slab, acc);
     return cudaGetLastError();
 }
 
