@@ -566,17 +566,20 @@ constexpr int kRowLanes = 8;   // lanes per weight row
 constexpr int kLaneCols = 16;  // consecutive block columns per lane
 constexpr int kBlockRows = kBlockThreads / kRowLanes;
 
-// One 128-column block of step 5.  Eight lanes hold one weight row, 16
-// consecutive block columns each (four rows per warp).  Column i is
-// quantized by the lane that holds it, its scaled error
-// err = (w - q) / U_ii is broadcast to the row's lanes, and every lane
-// applies w_j -= err * U_ij to its columns (U_ij = 0 for j < i, so columns
-// already quantized keep their value; the lane then parks err in the slot of
-// column i).  The code is rint(w / s) with w / s rounded to nearest as an
-// fp32 division: w * (1/s) is used unless it lies within 1e-4 of a half
-// integer, where the correctly rounded quotient decides.  Grouped blocks
-// take their scale from the block's values as they stand when the block
-// starts.
+// One 128-column block of step 5.  Eight lanes hold one weight row (four
+// rows per warp); lane l holds block columns 32t + 4l + u (t, u = 0..3), so
+// every row-of-U load and every global access of the eight lanes covers 128
+// contiguous bytes.  Column i is quantized by the lane that holds it, its
+// scaled error err = (w - q) / U_ii is broadcast to the row's lanes, and
+// every lane applies w_j -= err * U_ij to its columns (U_ij = 0 for j < i, so
+// columns already quantized keep their value; the owner then parks err in
+// the slot of column i).  Every lane evaluates the quantizer on its own slot
+// and only the owner's result is used, so the common path has no divergent
+// branch.  The code is rint(w / s) with w / s rounded to nearest as an fp32
+// division: w * (1/s) is used unless it lies within 1e-4 of a half integer,
+// where the correctly rounded quotient decides (a warp-uniform, rarely taken
+// branch).  Grouped blocks take their scale from the block's values as they
+// stand when the block starts.
 __global__ void __launch_bounds__(kBlockThreads) gq_block_kernel(const BlockArgs a) {
     extern __shared__ float4 us4[];  // U[b0:b0+128, b0:b0+128], row-major
     __shared__ float inv_u[kNB];
@@ -596,12 +599,11 @@ __global__ void __launch_bounds__(kBlockThreads) gq_block_kernel(const BlockArgs
          base += static_cast<int64_t>(gridDim.x) * kBlockRows) {
         const int64_t r = base + threadIdx.x / kRowLanes;
         const bool ok = r < a.rows;
-        float w[kLaneCols];
+        float w[kLaneCols];  // slot 4t + u <-> block column 32t + 4 sl + u
         if (ok) {
-            const float4* src = reinterpret_cast<const float4*>(a.Wc + r * a.d + b0 + kLaneCols * sl);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const float4 v = src[t];
+                const float4 v = *reinterpret_cast<const float4*>(a.Wc + r * a.d + b0 + 32 * t + 4 * sl);
                 w[4 * t] = v.x;
                 w[4 * t + 1] = v.y;
                 w[4 * t + 2] = v.z;
@@ -622,50 +624,54 @@ __global__ void __launch_bounds__(kBlockThreads) gq_block_kernel(const BlockArgs
             s = ok ? a.rowscale[r] : 1.0f;
         }
         const float inv_s = __frcp_rn(s);
-        uint32_t cw[kLaneCols / 4] = {0u, 0u, 0u, 0u};
+        uint32_t cw[4] = {0u, 0u, 0u, 0u};
         float lf = 0.0f;
-        for (int so = 0; so < kRowLanes; ++so) {
 #pragma unroll
-            for (int k = 0; k < kLaneCols; ++k) {
-                const int i = so * kLaneCols + k;
-                float err = 0.0f;
-                if (sl == so) {
+        for (int t = 0; t < 4; ++t) {
+            for (int so = 0; so < kRowLanes; ++so) {
+                const bool own = sl == so;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 4 * t + u;
+                    const int i = 32 * t + 4 * so + u;
+                    // every lane evaluates its slot k; the owner's result counts
                     const float x = w[k];
                     const float y = __fmul_rn(x, inv_s);
                     float q = rintf(y);
-                    if (fabsf(fabsf(__fsub_rn(y, q)) - 0.5f) < 1e-4f) q = rintf(__fdiv_rn(x, s));
+                    const bool tie = fabsf(fabsf(__fsub_rn(y, q)) - 0.5f) < 1e-4f;
+                    if (__any_sync(kFull, tie && own)) {
+                        if (tie && own) q = rintf(__fdiv_rn(x, s));
+                    }
                     q = fminf(fmaxf(q, -8.0f), 7.0f);
-                    err = __fmul_rn(__fsub_rn(x, __fmul_rn(s, q)), inv_u[i]);
-                    lf = fmaf(err, err, lf);
-                    cw[k >> 2] |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xffu) << (8 * (k & 3));
-                }
-                err = __shfl_sync(kFull, err, grp | so);
-                const float4* up = reinterpret_cast<const float4*>(Us + i * kNB + kLaneCols * sl);
+                    const float e = __fmul_rn(__fsub_rn(x, __fmul_rn(s, q)), inv_u[i]);
+                    lf = own ? fmaf(e, e, lf) : lf;
+                    cw[t] |= own ? (static_cast<uint32_t>(static_cast<int>(q)) & 0xffu) << (8 * u) : 0u;
+                    const float err = __shfl_sync(kFull, e, grp | so);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float4 u = up[t];
-                    w[4 * t] = __fsub_rn(w[4 * t], __fmul_rn(err, u.x));
-                    w[4 * t + 1] = __fsub_rn(w[4 * t + 1], __fmul_rn(err, u.y));
-                    w[4 * t + 2] = __fsub_rn(w[4 * t + 2], __fmul_rn(err, u.z));
-                    w[4 * t + 3] = __fsub_rn(w[4 * t + 3], __fmul_rn(err, u.w));
+                    for (int tt = 0; tt < 4; ++tt) {
+                        const float4 uv = *reinterpret_cast<const float4*>(Us + i * kNB + 32 * tt + 4 * sl);
+                        w[4 * tt] = __fsub_rn(w[4 * tt], __fmul_rn(err, uv.x));
+                        w[4 * tt + 1] = __fsub_rn(w[4 * tt + 1], __fmul_rn(err, uv.y));
+                        w[4 * tt + 2] = __fsub_rn(w[4 * tt + 2], __fmul_rn(err, uv.z));
+                        w[4 * tt + 3] = __fsub_rn(w[4 * tt + 3], __fmul_rn(err, uv.w));
+                    }
+                    w[k] = own ? err : w[k];
                 }
-                if (sl == so) w[k] = err;
             }
         }
         if (ok) {
-            float4* ep = reinterpret_cast<float4*>(a.Err + r * a.ld_err + kLaneCols * sl);
-            float4* qp = reinterpret_cast<float4*>(a.Wq + r * a.d + b0 + kLaneCols * sl);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                ep[t] = make_float4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+                const int c = 32 * t + 4 * sl;
+                *reinterpret_cast<float4*>(a.Err + r * a.ld_err + c) =
+                    make_float4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
                 float qf[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     qf[u] = __fmul_rn(s, static_cast<float>(static_cast<signed char>((cw[t] >> (8 * u)) & 0xffu)));
-                qp[t] = make_float4(qf[0], qf[1], qf[2], qf[3]);
+                *reinterpret_cast<float4*>(a.Wq + r * a.d + b0 + c) = make_float4(qf[0], qf[1], qf[2], qf[3]);
+                if (a.codes) *reinterpret_cast<uint32_t*>(a.codes + r * a.d + b0 + c) = cw[t];
             }
-            if (a.codes)
-                *reinterpret_cast<uint4*>(a.codes + r * a.d + b0 + kLaneCols * sl) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             if (a.grouped && sl == 0) a.scales[r * a.n_groups + a.b] = s;
             lsum += static_cast<double>(lf);
         }
