@@ -311,9 +311,15 @@ def _e2e(h, wl, xs, d, args, chunk_bytes=64 << 20):
                    "overlapped with the flushes"}
 
 
+# Secondary measurements, each with its own roofline; `--only NAME` runs one.
 def _extra(args, hbm, bf16_burst, bf16_sust):
-    """Secondary workloads: the compute-bound large-batch Gram and the
-    HBM-bound local 16x16 blocks, each with its own roofline."""
+    out = {}
+    for name, fn in EXTRAS.items():
+        out[name] = fn(hbm, bf16_burst)
+    return out
+
+
+def _x_large_batch_gram(hbm, bf16_burst):
     import torch
 
     from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
@@ -341,7 +347,15 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
         "roofline": {"bound": "tensor", "peak": bf16_burst, "unit": "TFLOP/s",
                      "frac": round(fl / t / 1e12 / bf16_burst, 4), "peak_source": "bf16_tflops (burst)"}}
     h.close()
-    del xs
+    return out["large_batch_gram"]
+
+
+def _x_flush_per_call(hbm, bf16_burst):
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    out = {}
     # the ragged stream flushed after every batch (no queue fusion): each call
     # reads its X and read-modify-writes the upper triangle of H
     wl = WORKLOADS["d4096_ragged360_loguniform"].scaled(n_batches=60)
@@ -364,7 +378,15 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "bytes_counted": "2*n*d + 8*d(d+1)/2 per call (X once, fp32 upper-triangle read+write)",
                      "fp64_tile_bytes_per_s_GB": round(acc_bytes / t / 1e9, 1)}}
     h.close()
-    del xs
+    return out["flush_per_call"]
+
+
+def _x_f32_input_ragged(hbm, bf16_burst):
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    out = {}
     # fp32-input path on the ragged d = 4096 stream (split-tf32 kernel)
     wl = WORKLOADS["d4096_ragged360_loguniform"]
     xs = [wl.batch(b, device="cuda", dtype=torch.float32) for b in range(len(wl.token_counts))]
@@ -386,7 +408,15 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "unit": "TFLOP/s", "frac": round(4 * fl / t / 1e12 / tf32_peak, 4),
                      "peak_source": "bf16_tflops (burst) x 1/2 (nominal tf32:bf16 ratio)"}}
     h.close()
-    del xs
+    return out["f32_input_ragged"]
+
+
+def _x_imatrix(hbm, bf16_burst):
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    out = {}
     # imatrix column sums of squares over the same local workload's batches
     wl = WORKLOADS["local_d4096_8x32768"]
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
@@ -412,7 +442,15 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
         "roofline": {"bound": "hbm", "achieved": round(nbytes / per / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(nbytes / per / 1e9 / hbm, 4), "kernel": "colsumsq_kernel"}}
     im.close()
-    del xs
+    return out["imatrix"]
+
+
+def _x_local_hessian(hbm, bf16_burst):
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    out = {}
     # local_hessian: 8 updates of 32768 tokens at d = 4096
     wl = WORKLOADS["local_d4096_8x32768"]
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
@@ -438,9 +476,7 @@ def _extra(args, hbm, bf16_burst, bf16_sust):
                      "unit": "GB/s", "frac": round(nbytes / per / 1e9 / hbm, 4),
                      "bytes_per_update": nbytes, "kernel": "local_gram_kernel"}}
     lh.close()
-    del xs
-    out["quantize_pass"] = _quantize_pass()
-    return out
+    return out["local_hessian"]
 
 
 # fp32 FMA lanes of GB300: 152 SMs x 128 lanes x 2 flops at the 2,070 MHz
@@ -492,6 +528,51 @@ def _quantize_pass(d=4096, rows=4096, reps=3):
                      "frac": round((f_prep + f_quant) / (tp + tq) / 1e12 / FP32_ALU_TFLOPS, 4),
                      "peak_source": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz",
                      "flops_counted": "2 d^3 / 3 (Cholesky + triangular inverse) + rows d (d-1)"}}
+
+
+def _x_merge(hbm, bf16_burst, d=4096, reps=5):
+    """hess_merge at d = 4,096: dst += src over the fp64 upper-triangle
+    tiles (69 MB each; 2 reads and 1 write per element)."""
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    wl = WORKLOADS["d4096_ragged360_loguniform"].scaled(n_batches=2)
+    a, b = Hessian(d), Hessian(d)
+    for k in range(2):
+        (a if k == 0 else b).add_batch(wl.batch(k, device="cuda"))
+    a.flush()
+    b.flush()
+    a.merge(b)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        a.merge(b)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(ts)
+    T = (d + 127) // 128
+    nbytes = 3 * T * (T + 1) // 2 * 128 * 128 * 8
+    a.close()
+    b.close()
+    return {"workload": f"hess_merge at d={d} (fp64 upper-triangle tiles)", "us_per_merge": round(t * 1e6, 2),
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(nbytes / t / 1e9 / hbm, 4), "bytes_per_merge": nbytes,
+                         "kernel": "add_f64_kernel"}}
+
+
+EXTRAS = {
+    "large_batch_gram": _x_large_batch_gram,
+    "flush_per_call": _x_flush_per_call,
+    "f32_input_ragged": _x_f32_input_ragged,
+    "imatrix": _x_imatrix,
+    "local_hessian": _x_local_hessian,
+    "merge": _x_merge,
+    "quantize_pass": lambda hbm, bf16_burst: _quantize_pass(),
+}
 
 
 # --------------------------------------------------------------- reference
@@ -590,8 +671,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-batches", type=int, default=2)
-    ap.add_argument("--quantize-only", action="store_true",
-                    help="run only the quantization-pass measurement and print its JSON")
+    ap.add_argument("--only", default=None,
+                    help="run one secondary measurement (large_batch_gram, flush_per_call, f32_input_ragged, "
+                         "imatrix, local_hessian, merge, quantize_pass) and print its JSON")
+    ap.add_argument("--quantize-only", action="store_true", help="same as --only quantize_pass")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -601,8 +684,12 @@ def main():
     else:
         from gptq_qqq_calibration_gb300 import build as b
         b.build()
-        if args.quantize_only:
-            print(json.dumps({"quantize_pass": _quantize_pass()}))
+        only = "quantize_pass" if args.quantize_only else args.only
+        if only:
+            if only not in EXTRAS:
+                raise SystemExit(f"--only: unknown measurement {only!r}; one of {sorted(EXTRAS)}")
+            hbm, bf16_burst, _, _ = peaks()
+            print(json.dumps({only: EXTRAS[only](hbm, bf16_burst)}))
         else:
             run_ours(args)
 
