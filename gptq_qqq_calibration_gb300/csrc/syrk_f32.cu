@@ -12,10 +12,10 @@
 // How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
 //   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
 //     128-byte swizzle with 32-byte granules, the layout MN-major tf32
-//     operands need) into a 3-deep landing ring; the whole of warp 0 then
-//     converts each landed stage into hi / lo planes of a 2-deep MMA ring,
-//     at the same byte offsets (so the swizzle carries over), and refills
-//     the landing slot at once;
+//     operands need) into a 3-deep landing ring; three converter warps
+//     (warp 0 and warps 10-11) turn each landed stage into hi / lo planes of
+//     a 2-deep MMA ring, at the same byte offsets (so the swizzle carries
+//     over), and warp 0 refills a landing slot once all three have read it;
 //   * warp 1 issues tcgen05.mma kind::tf32 (M=N=128, K=8): hi*hi into bank 0
 //     and the three small terms into bank 1, so they never ride on the
 //     large running sum;
@@ -40,7 +40,11 @@ constexpr uint32_t kBoxBytes = kKB * 128;           // 32 tokens x 32 fp32
 constexpr uint32_t kOpBytes = 4 * kBoxBytes;        // 128 features
 constexpr uint32_t kLandBytes = 2 * kOpBytes;       // A | B raw
 constexpr uint32_t kCvtBytes = 4 * kOpBytes;        // A hi | A lo | B hi | B lo
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+// Converters: warp 0 (also the TMA producer) and the two warps after the
+// epilogue warps; each takes every kCvtWarps-th round of 256 words.
+constexpr int kCvtWarps = 3;
+constexpr int kFirstExtraCvt = 2 + kEpiWarps;  // warps 10 and 11
+constexpr int kThreads = (2 + kEpiWarps + kCvtWarps - 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(2u /*tf32*/, 128, 128);
 constexpr int kNumBarriers = 2 * kLand + 2 * kCvt + 5;
@@ -107,14 +111,18 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
     auto accf_bar = [&](int b) { return bar0 + 8u * (kLand + 2 * kCvt + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (kLand + 2 * kCvt + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (kLand + 2 * kCvt + 4);
+    auto land_empty = [&](int s) { return bar0 + 8u * (kLand + 2 * kCvt + 5 + s); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kLand; ++s) mbar_init(land_full(s), 1);
+        for (int s = 0; s < kLand; ++s) {
+            mbar_init(land_full(s), 1);
+            mbar_init(land_empty(s), kCvtWarps);
+        }
         for (int s = 0; s < kCvt; ++s) {
-            mbar_init(cvt_full(s), 1);
+            mbar_init(cvt_full(s), kCvtWarps);
             mbar_init(cvt_empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -134,15 +142,67 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const unsigned long long limit = p.timeout_ns;
 
+    // Converter `ci` (0..kCvtWarps-1) splits its rounds of landed stage
+    // number `converted` (unit C) into hi / lo planes, then signals the MMA
+    // issuer (cvt_full) and the producer (land_empty).
+    auto convert_stage = [&](int ci, const Cursor& C, uint32_t converted) -> bool {
+        const int s = converted % kLand;
+        const int c = converted % kCvt;
+        if (!mbar_wait(land_full(s), (converted / kLand) & 1u, limit) ||
+            !mbar_wait(cvt_empty(c), ((converted / kCvt) & 1u) ^ 1u, limit))
+            return false;
+        const bool diag = C.un.I == C.un.J;
+        constexpr int kRoundsPerOp = static_cast<int>(kOpBytes / 16 / 256);  // 256 words per round
+        const int n_rounds = (diag ? 1 : 2) * kRoundsPerOp;
+        const uint32_t src = base + s * kLandBytes;
+        const uint32_t dst = base + kCvtBase + c * kCvtBytes;
+#pragma unroll 1
+        for (int rr = ci; rr < n_rounds; rr += kCvtWarps) {
+            const int op = rr / kRoundsPerOp, r = rr % kRoundsPerOp;
+            const uint32_t sp = src + op * kOpBytes;
+            const uint32_t hp = dst + op * 2 * kOpBytes;
+            const uint32_t lp = hp + kOpBytes;
+            uint4 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = lds128(sp + ((r * 8 + k) * 32 + lane) * 16);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t off = ((r * 8 + k) * 32 + lane) * 16;
+                float h0, h1, h2, h3, l0, l1, l2, l3;
+                split_tf32(__uint_as_float(x[k].x), h0, l0);
+                split_tf32(__uint_as_float(x[k].y), h1, l1);
+                split_tf32(__uint_as_float(x[k].z), h2, l2);
+                split_tf32(__uint_as_float(x[k].w), h3, l3);
+                sts128(hp + off, make_uint4(__float_as_uint(h0), __float_as_uint(h1),
+                                            __float_as_uint(h2), __float_as_uint(h3)));
+                sts128(lp + off, make_uint4(__float_as_uint(l0), __float_as_uint(l1),
+                                            __float_as_uint(l2), __float_as_uint(l3)));
+            }
+        }
+        // generic-proxy writes (and reads of the landing slot) must be
+        // visible to / ordered before the async proxy (MMA, next TMA)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(cvt_full(c));
+            mbar_arrive(land_empty(s));
+        }
+        return true;
+    };
+
     if (warp == 0) {
-        // ---------------------------------- TMA producer + tf32 splitter
+        // ---------------------------------- TMA producer + converter 0
         bool ok = true;
         Cursor L, C;
         cursor_start(p, L);
         cursor_start(p, C);
         uint32_t issued = 0, converted = 0;
-        auto issue = [&]() {
+        auto issue = [&]() -> bool {
             const int s = issued % kLand;
+            // a reused landing slot must have been read by every converter
+            if (issued >= static_cast<uint32_t>(kLand) &&
+                !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit))
+                return false;
             const bool diag = L.un.I == L.un.J;
             if (lane == 0) {
                 const CUtensorMap* m = &p.maps[L.b];
@@ -156,55 +216,20 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
                         tma_load_2d(dst + kOpBytes + bx * kBoxBytes, m, land_full(s),
                                     L.un.J * kTile + 32 * bx, tok);
             }
+            __syncwarp();
             ++issued;
             cursor_next(p, L);
+            return true;
         };
         while (L.valid && issued < static_cast<uint32_t>(kLand)) issue();
         while (ok && C.valid) {
-            const int s = converted % kLand;
-            const int c = converted % kCvt;
-            if (!mbar_wait(land_full(s), (converted / kLand) & 1u, limit) ||
-                !mbar_wait(cvt_empty(c), ((converted / kCvt) & 1u) ^ 1u, limit)) {
+            if (!convert_stage(0, C, converted)) {
                 ok = false;
                 break;
             }
-            const bool diag = C.un.I == C.un.J;
-            const int n_ops = diag ? 1 : 2;
-            const uint32_t src = base + s * kLandBytes;
-            const uint32_t dst = base + kCvtBase + c * kCvtBytes;
-            for (int op = 0; op < n_ops; ++op) {
-                const uint32_t sp = src + op * kOpBytes;
-                const uint32_t hp = dst + op * 2 * kOpBytes;
-                const uint32_t lp = hp + kOpBytes;
-                // 1,024 16-byte words per operand, 8 per lane per round, 4 rounds
-#pragma unroll 1
-                for (int r = 0; r < static_cast<int>(kOpBytes / 16 / 256); ++r) {
-                    uint4 x[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[k] = lds128(sp + ((r * 8 + k) * 32 + lane) * 16);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = ((r * 8 + k) * 32 + lane) * 16;
-                        float h0, h1, h2, h3, l0, l1, l2, l3;
-                        split_tf32(__uint_as_float(x[k].x), h0, l0);
-                        split_tf32(__uint_as_float(x[k].y), h1, l1);
-                        split_tf32(__uint_as_float(x[k].z), h2, l2);
-                        split_tf32(__uint_as_float(x[k].w), h3, l3);
-                        sts128(hp + off, make_uint4(__float_as_uint(h0), __float_as_uint(h1),
-                                                    __float_as_uint(h2), __float_as_uint(h3)));
-                        sts128(lp + off, make_uint4(__float_as_uint(l0), __float_as_uint(l1),
-                                                    __float_as_uint(l2), __float_as_uint(l3)));
-                    }
-                }
-            }
-            // generic-proxy writes (and reads of the landing slot) must be
-            // visible to / ordered before the async proxy (MMA, next TMA)
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cvt_full(c));
             ++converted;
             cursor_next(p, C);
-            if (L.valid) issue();
+            if (L.valid && !issue()) ok = false;
         }
         if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
         // Every issued copy must land before the CTA may exit.
@@ -216,6 +241,22 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
                 }
             }
         }
+    } else if (warp >= kFirstExtraCvt) {
+        // ---------------------------------- converters 1 and 2
+        const int ci = warp - kFirstExtraCvt + 1;
+        Cursor C;
+        cursor_start(p, C);
+        uint32_t converted = 0;
+        bool ok = true;
+        while (ok && C.valid) {
+            if (!convert_stage(ci, C, converted)) {
+                ok = false;
+                break;
+            }
+            ++converted;
+            cursor_next(p, C);
+        }
+        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -276,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
     } else {
-        // ------------------------------------------------ epilogue (8 warps)
+        // ------------------------------------------------ epilogue (warps 2-9)
         syrk::epilogue<kExcl>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
     }
 
