@@ -20,7 +20,7 @@ OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgptq_hess.so")
 
 SOURCES = ["syrk_bf16.cu", "syrk_bf16_2sm.cu", "syrk_f32.cu", "local_gram.cu", "materialize.cu", "hess_api.cu", "gptq.cu",
-           "local_noalloc.cu", "stats.cu"]
+           "local_noalloc.cu", "stats.cu", "gemm_tf32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC]

@@ -45,6 +45,7 @@ constexpr int kBlockThreads = 128;
 constexpr int kSuper = 4;          // blocks per lazy super-block of step 5
 constexpr size_t kBlockSmem = kNB * kNB * sizeof(float);
 constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned long long kGemmTimeoutNs = 2000000000ull;  // bound of every wait in the tensor GEMM
 
 // ------------------------------------------------------------- steps 2-3
 
@@ -555,11 +556,11 @@ struct BlockArgs {
     float* Wq;              // rows x d dequantized output
     signed char* codes;     // rows x d codes or NULL
     float* scales;          // rows x n_groups
-    float* Err;             // scaled errors of this block: rows x 128 at stride ld_err
+    float* ErrT;            // scaled errors of this block, transposed: 128 x rows at stride ld_errt
     const float* rowscale;  // whole-row scales (grouped == 0)
     double* loss;
     int64_t rows;
-    int d, b, n_groups, grouped, ld_err;
+    int d, b, n_groups, grouped, ld_errt;
 };
 
 constexpr int kRowLanes = 8;   // lanes per weight row
@@ -663,8 +664,8 @@ __global__ void __launch_bounds__(kBlockThreads) gq_block_kernel(const BlockArgs
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int c = 32 * t + 4 * sl;
-                *reinterpret_cast<float4*>(a.Err + r * a.ld_err + c) =
-                    make_float4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) a.ErrT[static_cast<size_t>(c + u) * a.ld_errt + r] = w[4 * t + u];
                 float qf[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -742,7 +743,8 @@ struct gptq_ctx {
     float* X = nullptr;         // d x d: inv(L) workspace
     float* Dinv = nullptr;      // n_blocks x 128 x 128 inverses of the diagonal blocks
     float* Wc = nullptr;        // max_rows x d working matrix
-    float* Err = nullptr;       // max_rows x (kSuper * 128) errors of one super-block
+    float* ErrT = nullptr;      // (kSuper * 128) x ld_errt: errors of one super-block, transposed
+    int ld_errt = 0;            // max_rows rounded up to a multiple of 4 (16-byte rows)
     float* rowscale = nullptr;  // max_rows
     unsigned char* dead = nullptr;
     double* damp64 = nullptr;
@@ -771,7 +773,7 @@ void gq_free(gptq_ctx* g) {
     cudaFree(g->X);
     cudaFree(g->Dinv);
     cudaFree(g->Wc);
-    cudaFree(g->Err);
+    cudaFree(g->ErrT);
     cudaFree(g->rowscale);
     cudaFree(g->dead);
     cudaFree(g->damp64);
@@ -887,13 +889,17 @@ GQ_EXPORT hess_status gptq_create(int64_t d, int64_t max_rows, gptq_t* out) {
     if (e == cudaSuccess) e = cudaMalloc(&g->X, dd * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->Dinv, static_cast<size_t>(d) * kNB * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->Wc, rows * d * sizeof(float));
-    if (e == cudaSuccess) e = cudaMalloc(&g->Err, rows * kSuper * kNB * sizeof(float));
+    g->ld_errt = static_cast<int>((rows + 3) / 4 * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&g->ErrT, static_cast<size_t>(kSuper) * kNB * g->ld_errt * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->rowscale, rows * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->dead, static_cast<size_t>(d));
     if (e == cudaSuccess) e = cudaMalloc(&g->damp64, sizeof(double));
     if (e == cudaSuccess) e = cudaMalloc(&g->damp32, sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&g->loss, sizeof(double));
-    if (e == cudaSuccess) e = cudaMalloc(&g->status, sizeof(int));
+    // status[0]: Cholesky pivot flag; status[1]: device-side wait limits of the tensor GEMM
+    if (e == cudaSuccess) e = cudaMalloc(&g->status, 4 * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(g->status, 0, 4 * sizeof(int));
+    if (e == cudaSuccess) e = hk::gemm_tf32_prepare();
     if (e == cudaSuccess) e = cudaMalloc(&g->Mk, static_cast<size_t>(d) * kNB * sizeof(float));
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g->side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_fork, cudaEventDisableTiming);
@@ -982,6 +988,7 @@ GQ_EXPORT hess_status gptq_quantize(gptq_t g, const void* W, int32_t w_dtype, in
     const int d = static_cast<int>(g->d), n = g->n_blocks;
     const bool grouped = group_size == kNB;
     GQ_TRY(cudaMemsetAsync(g->loss, 0, sizeof(double), s));
+    GQ_TRY(cudaMemsetAsync(g->status + 1, 0, sizeof(int), s));
     if (rows > 0) {
         const size_t n4 = static_cast<size_t>(rows) * d / 4;
         if (w_dtype == HESS_F32)
@@ -998,35 +1005,41 @@ GQ_EXPORT hess_status gptq_quantize(gptq_t g, const void* W, int32_t w_dtype, in
         }
         const int wanted = static_cast<int>((rows + kBlockRows - 1) / kBlockRows);
         const int grid = std::min(wanted, 3 * g->sm_count);
-        const int ld_err = kSuper * kNB;
-        // Two-level lazy update: after each block only the rest of its
-        // super-block (kSuper blocks) is updated; the columns after the
-        // super-block get one K = kSuper * 128 update.
+        const int ldt = g->ld_errt;
+        uint32_t* gemm_status = reinterpret_cast<uint32_t*>(g->status) + 1;
+        // Two-level lazy update on the tensor cores (C -= P^T Q with P the
+        // transposed errors and Q a panel of U): after each block only the
+        // rest of its super-block (kSuper blocks) is updated; the columns
+        // after the super-block get one K = kSuper * 128 update.
         for (int sb0 = 0; sb0 < n; sb0 += kSuper) {
             const int sb1 = std::min(n, sb0 + kSuper);
             for (int b = sb0; b < sb1; ++b) {
-                float* err_b = g->Err + (b - sb0) * kNB;
-                BlockArgs a{g->Wc, g->F, Wq_out, reinterpret_cast<signed char*>(codes_out), scales_out, err_b,
-                            g->rowscale, g->loss, rows, d, b, grouped ? n : 1, grouped ? 1 : 0, ld_err};
+                float* errt_b = g->ErrT + static_cast<size_t>(b - sb0) * kNB * ldt;
+                BlockArgs a{g->Wc, g->F, Wq_out, reinterpret_cast<signed char*>(codes_out), scales_out, errt_b,
+                            g->rowscale, g->loss, rows, d, b, grouped ? n : 1, grouped ? 1 : 0, ldt};
                 gq_block_kernel<<<grid, kBlockThreads, kBlockSmem, s>>>(a);
                 GQ_TRY(cudaGetLastError());
                 const int in_super = (sb1 - b - 1) * kNB;  // columns left in this super-block
                 if (in_super > 0)
-                    GQ_TRY(gemm<false>(g->sm_count, err_b, ld_err, g->F + static_cast<size_t>(b) * kNB * d + (b + 1) * kNB, d,
-                                       g->Wc + (b + 1) * kNB, d, static_cast<int>(rows), in_super, kNB, -1.0f, 1, 0,
-                                       s));
+                    GQ_TRY(hk::launch_gemm_tf32(errt_b, ldt, g->F + static_cast<size_t>(b) * kNB * d + (b + 1) * kNB,
+                                                d, g->Wc + (b + 1) * kNB, d, static_cast<int>(rows), in_super, kNB,
+                                                -1.0f, gemm_status, kGemmTimeoutNs, g->sm_count, s));
             }
             const int rest = d - sb1 * kNB;
             if (rest > 0)
-                GQ_TRY(gemm<false>(g->sm_count, g->Err, ld_err, g->F + static_cast<size_t>(sb0) * kNB * d + sb1 * kNB, d,
-                                   g->Wc + sb1 * kNB, d, static_cast<int>(rows), rest, (sb1 - sb0) * kNB, -1.0f, 1,
-                                   0, s));
+                GQ_TRY(hk::launch_gemm_tf32(g->ErrT, ldt, g->F + static_cast<size_t>(sb0) * kNB * d + sb1 * kNB, d,
+                                            g->Wc + sb1 * kNB, d, static_cast<int>(rows), rest, (sb1 - sb0) * kNB,
+                                            -1.0f, gemm_status, kGemmTimeoutNs, g->sm_count, s));
         }
     }
     if (avg_loss_out) {
         double loss = 0.0;
+        int gst = 0;
         GQ_TRY(cudaMemcpyAsync(&loss, g->loss, sizeof(double), cudaMemcpyDeviceToHost, s));
+        GQ_TRY(cudaMemcpyAsync(&gst, g->status + 1, sizeof(int), cudaMemcpyDeviceToHost, s));
         GQ_TRY(cudaStreamSynchronize(s));
+        if (gst != 0)
+            return gq_fail(HESS_ERR_TIMEOUT, "a device-side wait of the tensor-core GEMM ran out (status 0x%x)", gst);
         *avg_loss_out = g->n_tokens > 0 ? loss / static_cast<double>(g->n_tokens) : loss;
     }
     return HESS_OK;

@@ -74,6 +74,28 @@ __host__ __device__ inline int pair_tile_count(int T) {
     return n;
 }
 
+// Tensor-core fp32 GEMM C[M x N] += alpha P^T Q (gemm_tf32.cu); P is K x M and
+// Q is K x N, both row-major with the minor dimension contiguous.
+struct GemmTf32Params {
+    CUtensorMap p_map;  // P: dims {M, K}, 32 x 32 boxes, fp32, 128B swizzle with 32B atoms
+    CUtensorMap q_map;  // Q: dims {N, K}
+    float* C;
+    int32_t ldc, M, N, K;
+    float alpha;
+    int32_t tiles_n;  // N / 128
+    int32_t n_kb;     // K / 32
+    int32_t n_units;  // tiles_n * ceil(M / 128)
+    uint32_t* status;
+    unsigned long long timeout_ns;
+};
+size_t gemm_tf32_smem_bytes();
+cudaError_t gemm_tf32_prepare();
+// Encodes the tensor maps and launches.  P, Q, C 16-byte aligned; ldp, ldq,
+// ldc multiples of 4; N % 128 == 0; K % 32 == 0; M >= 1.
+cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, float* C, int ldc, int M, int N,
+                             int K, float alpha, uint32_t* status, unsigned long long timeout_ns, int grid_max,
+                             cudaStream_t s);
+
 size_t syrk_f32_smem_bytes();
 cudaError_t syrk_f32_prepare();
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
