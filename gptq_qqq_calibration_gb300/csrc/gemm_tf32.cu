@@ -76,6 +76,20 @@ __device__ __forceinline__ void cur_next(const GemmTf32Params& p, Cursor& c) {
     c.valid = c.u < p.n_units;
 }
 
+// First C column (n0) and row (m0) of tile u.
+__device__ __forceinline__ void unit_tile(const GemmTf32Params& p, int u, int& n0, int& m0) {
+    if (p.lower) {  // u = a (a + 1) / 2 + b, b <= a: row tile a, column tile b
+        int a = static_cast<int>((sqrtf(8.0f * u + 1.0f) - 1.0f) * 0.5f);
+        while (a * (a + 1) / 2 > u) --a;
+        while ((a + 1) * (a + 2) / 2 <= u) ++a;
+        n0 = (u - a * (a + 1) / 2) * 128;
+        m0 = a * 128;
+    } else {
+        n0 = (u % p.tiles_n) * 128;
+        m0 = (u / p.tiles_n) * 128;
+    }
+}
+
 // hi = x rounded to nearest tf32 (low 13 bits cleared), lo = x - hi exactly.
 __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
     const uint32_t u = __float_as_uint(x);
@@ -186,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
                 !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit))
                 return false;
             if (lane == 0) {
-                const int n0 = (L.u % p.tiles_n) * 128;  // C columns (Q)
-                const int m0 = (L.u / p.tiles_n) * 128;  // C rows (P)
+                int n0, m0;  // first C column (Q) and row (P)
+                unit_tile(p, L.u, n0, m0);
                 const int k0 = L.kb * kKB;
                 const uint32_t dst = base + s * kLandBytes;
                 mbar_arrive_expect_tx(land_full(s), kLandBytes);
@@ -304,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
                 break;
             }
             tc_fence_after();
-            const int n0 = (u % p.tiles_n) * 128;
-            const int m0 = (u / p.tiles_n) * 128;
+            int n0, m0;
+            unit_tile(p, u, n0, m0);
             const int col = n0 + q * 32 + lane;
             const uint32_t tb = tmem + lane_off + static_cast<uint32_t>(ab) * 256u + part * 64u;
             // 32 rows per step: their 32 loads of C are in flight together
@@ -395,9 +409,10 @@ cudaError_t gemm_tf32_prepare() {
 
 cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, float* C, int ldc, int M, int N,
                              int K, float alpha, uint32_t* status, unsigned long long timeout_ns, int grid_max,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool lower) {
     if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
     if (N % 128 != 0 || K % kKB != 0 || ldp % 4 || ldq % 4 || ldc % 4) return cudaErrorInvalidValue;
+    if (lower && M != N) return cudaErrorInvalidValue;
     GemmTf32Params p{};
     cudaError_t e = encode_fp32(&p.p_map, P, M, K, ldp);
     if (e == cudaSuccess) e = encode_fp32(&p.q_map, Q, N, K, ldq);
@@ -410,7 +425,8 @@ cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, f
     p.alpha = alpha;
     p.tiles_n = N / 128;
     p.n_kb = K / kKB;
-    p.n_units = p.tiles_n * ((M + 127) / 128);
+    p.lower = lower ? 1 : 0;
+    p.n_units = lower ? p.tiles_n * (p.tiles_n + 1) / 2 : p.tiles_n * ((M + 127) / 128);
     p.status = status;
     p.timeout_ns = timeout_ns;
     const int grid = p.n_units < grid_max ? p.n_units : grid_max;

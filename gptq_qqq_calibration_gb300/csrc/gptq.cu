@@ -196,6 +196,7 @@ __device__ __forceinline__ bool potrf_sub_block(float* S, float* Xs, float* Yt, 
 
 __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __restrict__ F, int d, int k,
                                                                  float* __restrict__ Dinv,
+                                                                 float* __restrict__ DinvT,
                                                                  int* __restrict__ status) {
     extern __shared__ __align__(16) float sm[];
     float* S = sm;                  // [kNB][kLd]: the block, then L
@@ -372,6 +373,16 @@ __global__ void __launch_bounds__(kPotrfThreads, 1) gq_potrf_kernel(float* __res
         }
         *reinterpret_cast<float4*>(blk + static_cast<size_t>(i) * d + j) = make_float4(l[0], l[1], l[2], l[3]);
         *reinterpret_cast<float4*>(inv + i * kNB + j) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    // inv(L_kk)^T: row i holds column i of the inverse (nonzero from row i down).
+    float* invT = DinvT + static_cast<size_t>(k) * kNB * kNB;
+#pragma unroll 4
+    for (int it = 0; it < kVecPerThread; ++it) {
+        const int e4 = tid + it * kPotrfThreads, i = e4 >> 5, j = (e4 & 31) * 4;
+        float y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) y[u] = i <= j + u ? Xs[(j + u) * kLd + i] : 0.0f;
+        *reinterpret_cast<float4*>(invT + i * kNB + j) = make_float4(y[0], y[1], y[2], y[3]);
     }
 }
 
@@ -751,9 +762,12 @@ struct gptq_ctx {
     float* damp32 = nullptr;
     double* loss = nullptr;
     int* status = nullptr;
-    float* Mk = nullptr;             // (d - 128) x 128: L_ik inv(L_kk) of one step
+    float* DinvT = nullptr;          // the inverses of the diagonal blocks, transposed
+    float* L21T[2] = {nullptr, nullptr};  // 128 x (d - 128): a step's panel, transposed (two steps in flight)
+    float* MkT = nullptr;            // 128 x (d - 128): (L_ik inv(L_kk))^T of one step
     cudaStream_t side = nullptr;     // inverse block rows, alongside the Cholesky
     cudaEvent_t ev_fork = nullptr, ev_panel = nullptr, ev_side = nullptr;
+    cudaEvent_t ev_l21t[2] = {nullptr, nullptr};  // the side stream has read panel buffer 0 / 1
     bool prepared = false;
     int64_t n_tokens = 0;
 };
@@ -780,7 +794,12 @@ void gq_free(gptq_ctx* g) {
     cudaFree(g->damp32);
     cudaFree(g->loss);
     cudaFree(g->status);
-    cudaFree(g->Mk);
+    cudaFree(g->DinvT);
+    cudaFree(g->L21T[0]);
+    cudaFree(g->L21T[1]);
+    cudaFree(g->MkT);
+    for (int i = 0; i < 2; ++i)
+        if (g->ev_l21t[i]) cudaEventDestroy(g->ev_l21t[i]);
     if (g->side) cudaStreamDestroy(g->side);
     if (g->ev_fork) cudaEventDestroy(g->ev_fork);
     if (g->ev_panel) cudaEventDestroy(g->ev_panel);
@@ -795,7 +814,7 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
     const int d = static_cast<int>(g->d), n = g->n_blocks;
     const size_t dd = static_cast<size_t>(d) * d;
     g->prepared = false;
-    GQ_TRY(cudaMemsetAsync(g->status, 0, sizeof(int), s));
+    GQ_TRY(cudaMemsetAsync(g->status, 0, 2 * sizeof(int), s));
     gq_damp_kernel<<<1, 1024, 0, s>>>(H, d, damp_percent, g->dead, g->damp64, g->damp32);
     GQ_TRY(cudaGetLastError());
     gq_rotate_in_kernel<<<stride_grid(dd / 4, g->sm_count), 256, 0, s>>>(H, g->F, d, g->dead, g->damp64);
@@ -813,25 +832,32 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
     GQ_TRY(cudaGetLastError());
     GQ_TRY(cudaEventRecord(g->ev_fork, s));
     GQ_TRY(cudaStreamWaitEvent(g->side, g->ev_fork, 0));
+    uint32_t* gemm_status = reinterpret_cast<uint32_t*>(g->status) + 1;
     for (int k = 0; k < n; ++k) {
-        gq_potrf_kernel<<<1, kPotrfThreads, kPotrfSmem, s>>>(g->F, d, k, g->Dinv, g->status);
+        gq_potrf_kernel<<<1, kPotrfThreads, kPotrfSmem, s>>>(g->F, d, k, g->Dinv, g->DinvT, g->status);
         GQ_TRY(cudaGetLastError());
         const int rem = d - (k + 1) * kNB;
         if (rem == 0) break;
-        float* A21 = g->F + static_cast<size_t>(k + 1) * kNB * d + static_cast<size_t>(k) * kNB;
+        const float* A21 = g->F + static_cast<size_t>(k + 1) * kNB * d + static_cast<size_t>(k) * kNB;
         float* A22 = g->F + static_cast<size_t>(k + 1) * kNB * (d + 1);
         const float* Dk = g->Dinv + static_cast<size_t>(k) * kNB * kNB;
-        // L21 = A21 inv(L11)^T, in place (one 128-wide column tile).
-        GQ_TRY(gemm<true>(g->sm_count, A21, d, Dk, kNB, A21, d, rem, kNB, kNB, 1.0f, 0, 0, s));
+        const float* DkT = g->DinvT + static_cast<size_t>(k) * kNB * kNB;
+        float* L21T = g->L21T[k & 1];  // 128 x rem, leading dimension rem
+        // The side stream reads a panel two steps before its buffer is reused.
+        if (k >= 2) GQ_TRY(cudaStreamWaitEvent(s, g->ev_l21t[k & 1], 0));
+        // L21^T = inv(L11) A21^T (CUDA cores; 128 rows).
+        GQ_TRY(gemm<true>(g->sm_count, Dk, kNB, A21, d, L21T, rem, kNB, rem, kNB, 1.0f, 0, 0, s));
         GQ_TRY(cudaEventRecord(g->ev_panel, s));
-        // A22 -= L21 L21^T on the tiles at or below the diagonal.
-        GQ_TRY(gemm<true>(g->sm_count, A21, d, A21, d, A22, d, rem, rem, kNB, -1.0f, 1, kGemmCLowerTiles, s));
-        // Side stream: M_k = L21 inv(L11), then B[k+1:, :k+1] -= M_k B_k.
+        // A22 -= L21 L21^T on the tensor cores, tiles at or below the diagonal.
+        GQ_TRY(hk::launch_gemm_tf32(L21T, rem, L21T, rem, A22, d, rem, rem, kNB, -1.0f, gemm_status,
+                                    kGemmTimeoutNs, g->sm_count, s, /*lower=*/true));
+        // Side stream: M_k^T = inv(L11)^T L21^T, then B[k+1:, :k+1] -= M_k B_k.
         GQ_TRY(cudaStreamWaitEvent(g->side, g->ev_panel, 0));
-        GQ_TRY(gemm<false>(g->sm_count, A21, d, Dk, kNB, g->Mk, kNB, rem, kNB, kNB, 1.0f, 0, 0, g->side));
+        GQ_TRY(gemm<false>(g->sm_count, DkT, kNB, L21T, rem, g->MkT, rem, kNB, rem, kNB, 1.0f, 0, 0, g->side));
+        GQ_TRY(cudaEventRecord(g->ev_l21t[k & 1], g->side));
         float* Bk = g->X + static_cast<size_t>(k) * kNB * d;
-        GQ_TRY(gemm<false>(g->sm_count, g->Mk, kNB, Bk, d, Bk + static_cast<size_t>(kNB) * d, d, rem, (k + 1) * kNB, kNB, -1.0f,
-                           1, 0, g->side));
+        GQ_TRY(hk::launch_gemm_tf32(g->MkT, rem, Bk, d, Bk + static_cast<size_t>(kNB) * d, d, rem, (k + 1) * kNB,
+                                    kNB, -1.0f, gemm_status, kGemmTimeoutNs, g->sm_count, g->side));
     }
     GQ_TRY(cudaEventRecord(g->ev_side, g->side));
     GQ_TRY(cudaStreamWaitEvent(s, g->ev_side, 0));
@@ -843,13 +869,16 @@ hess_status prepare_locked(gptq_ctx* g, const float* H, double damp_percent, cud
     // U = J X J into F.
     gq_reverse_copy_kernel<<<stride_grid(dd / 4, g->sm_count), 256, 0, s>>>(g->X, g->F, dd / 4);
     GQ_TRY(cudaGetLastError());
-    int status = 0;
+    int status[2] = {0, 0};
     float damp = 0.0f;
-    GQ_TRY(cudaMemcpyAsync(&status, g->status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    GQ_TRY(cudaMemcpyAsync(status, g->status, 2 * sizeof(int), cudaMemcpyDeviceToHost, s));
     GQ_TRY(cudaMemcpyAsync(&damp, g->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
     GQ_TRY(cudaStreamSynchronize(s));
     if (damp_out) *damp_out = damp;
-    if (status & 1)
+    if (status[1] != 0)
+        return gq_fail(HESS_ERR_TIMEOUT, "a device-side wait of the tensor-core GEMM ran out (status 0x%x)",
+                       status[1]);
+    if (status[0] & 1)
         return gq_fail(HESS_ERR_NOT_PD, "the damped Hessian is not positive definite in fp32 "
                                         "(a Cholesky pivot was <= 0 or not finite)");
     g->prepared = true;
@@ -900,7 +929,11 @@ GQ_EXPORT hess_status gptq_create(int64_t d, int64_t max_rows, gptq_t* out) {
     if (e == cudaSuccess) e = cudaMalloc(&g->status, 4 * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(g->status, 0, 4 * sizeof(int));
     if (e == cudaSuccess) e = hk::gemm_tf32_prepare();
-    if (e == cudaSuccess) e = cudaMalloc(&g->Mk, static_cast<size_t>(d) * kNB * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&g->DinvT, static_cast<size_t>(d) * kNB * sizeof(float));
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+        e = cudaMalloc(&g->L21T[i], static_cast<size_t>(d) * kNB * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&g->MkT, static_cast<size_t>(d) * kNB * sizeof(float));
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&g->ev_l21t[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g->side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->ev_panel, cudaEventDisableTiming);

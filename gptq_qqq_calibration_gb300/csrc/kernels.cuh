@@ -84,7 +84,8 @@ struct GemmTf32Params {
     float alpha;
     int32_t tiles_n;  // N / 128
     int32_t n_kb;     // K / 32
-    int32_t n_units;  // tiles_n * ceil(M / 128)
+    int32_t n_units;  // tiles_n * ceil(M / 128), or T (T + 1) / 2 tiles when lower
+    int32_t lower;    // 1: square C, only the 128 x 128 tiles at or below the diagonal
     uint32_t* status;
     unsigned long long timeout_ns;
 };
@@ -92,9 +93,11 @@ size_t gemm_tf32_smem_bytes();
 cudaError_t gemm_tf32_prepare();
 // Encodes the tensor maps and launches.  P, Q, C 16-byte aligned; ldp, ldq,
 // ldc multiples of 4; N % 128 == 0; K % 32 == 0; M >= 1.
+// `lower`: M == N and only the tiles at or below the diagonal are computed
+// (the diagonal tiles in full).
 cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, float* C, int ldc, int M, int N,
                              int K, float alpha, uint32_t* status, unsigned long long timeout_ns, int grid_max,
-                             cudaStream_t s);
+                             cudaStream_t s, bool lower = false);
 
 size_t syrk_f32_smem_bytes();
 cudaError_t syrk_f32_prepare();
