@@ -298,13 +298,33 @@ def _e2e(h, wl, xs, d, args, chunk_bytes=64 << 20):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
+    # the host link's rate at this moment: the same bytes as one plain copy
+    link = []
+    for _ in range(2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(copy_s)
+        with torch.cuda.stream(copy_s):
+            dev_buf.copy_(host_buf, non_blocking=True)
+        b.record(copy_s)
+        torch.cuda.synchronize()
+        link.append(total * row_bytes / (a.elapsed_time(b) * 1e-3) / 1e9)
     steps = max(3, args.steps // 2)
-    t0 = time.perf_counter()
+    # each step ends with a device -> host read that the next step's copies
+    # wait for anyway, so timing steps one by one costs nothing; it shows the
+    # host link's occasional stalls (100-160 ms, seen also with the copies
+    # alone) that a mean over the steps absorbs
+    per = []
     for _ in range(steps):
+        t0 = time.perf_counter()
         step()
-    torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / steps
+        torch.cuda.synchronize()
+        per.append(time.perf_counter() - t0)
+    dt = sum(per) / steps
+    med = statistics.median(per)
     return {"value": round(flops / dt / 1e12, 3), "unit": "TFLOP/s",
+            "median_step_ms": round(med * 1e3, 3), "median_tflops": round(flops / med / 1e12, 3),
+            "stalled_steps": int(sum(t > 2 * med for t in per)),
+            "h2d_link_gbs": round(max(link), 1),
             "h2d_bytes_per_step": int(total * row_bytes),
             "d2h_bytes_per_step": int(d * d * 4), "ms_per_step": round(dt * 1e3, 3),
             "h2d": f"one pinned buffer, {len(chunks)} chunks of ~{chunk_bytes >> 20} MB on a copy stream, "
