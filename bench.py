@@ -547,7 +547,9 @@ def _quantize_pass(d=4096, rows=4096, reps=3):
                      "achieved": round((f_prep + f_quant) / (tp + tq) / 1e12, 2),
                      "frac": round((f_prep + f_quant) / (tp + tq) / 1e12 / FP32_ALU_TFLOPS, 4),
                      "peak_source": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz",
-                     "flops_counted": "2 d^3 / 3 (Cholesky + triangular inverse) + rows d (d-1)"}}
+                     "flops_counted": "2 d^3 / 3 (Cholesky + triangular inverse) + rows d (d-1)",
+                     "note": "fp32 work; the large GEMMs run as split tf32 (3 MMAs per product) on the "
+                             "tensor cores, the diagonal blocks and step 5's column chain on CUDA cores"}}
 
 
 def _x_merge(hbm, bf16_burst, d=4096, reps=5):
