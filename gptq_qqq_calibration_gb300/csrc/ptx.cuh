@@ -38,25 +38,36 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// A waiting thread may sleep in try_wait until the phase completes or this
+// many nanoseconds pass, instead of polling (the caller still bounds the
+// total wait with the global timer).
+constexpr uint32_t kTryWaitSuspendNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
+}
+
+// Suspend hint of one try_wait within a wait bounded by limit_ns.
+__device__ __forceinline__ uint32_t try_wait_hint(uint64_t limit_ns) {
+    return limit_ns < kTryWaitSuspendNs ? static_cast<uint32_t>(limit_ns) : kTryWaitSuspendNs;
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed, or until
 // `limit_ns` nanoseconds have passed.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = try_wait_hint(limit_ns);
+    if (mbar_try_wait(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, hint)) return true;
         if (globaltimer_ns() - t0 >= limit_ns) return false;
     }
 }
@@ -309,23 +320,24 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 }
 
 // try_wait with acquire at cluster scope (for barriers a peer CTA arrives on).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint32_t hint = try_wait_hint(limit_ns);
+    if (mbar_try_wait_cluster(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (mbar_try_wait_cluster(bar, parity, hint)) return true;
         if (globaltimer_ns() - t0 >= limit_ns) return false;
     }
 }
