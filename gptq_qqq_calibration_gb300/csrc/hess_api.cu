@@ -3,7 +3,7 @@
 //
 // Queue: hess_add_batch only records (pointer, tokens, stream).  A flush
 // turns every queued batch of one dtype into one tensor map, concatenates
-// their tokens into one stream of 64-token k-blocks and runs a single
+// their tokens into one stream of 128-token k-blocks and runs a single
 // split-K SYRK pass over it, so the accumulator is read and written once per
 // flush instead of once per batch (GPTQModel PR #2981, Changes: no transient
 // d x d product per batch; the accumulator is allocated once).
@@ -173,20 +173,20 @@ hess_status check_device(int dev) {
 
 // Split-K factor (token slabs) from a per-unit cost model in SM cycles:
 // each unit costs max(MMA, epilogue), waves of units run back to back.  The
-// MMA part is ~300 cycles per 64-token k-block of a 128 x 128 tile; the
+// MMA part is ~4.7 cycles per token of a 128 x 128 tile; the
 // epilogue moves a 128 KB fp64 tile: ~12k cycles as a plain read-modify-
 // write (one slab, one writer per tile, HBM-bound) and ~36k with
 // red.add.f64 (several slabs; L2 applies fp64 adds at ~1.1 TB/s).  Small
 // flushes are epilogue-bound and take one slab; large ones split to fill
 // the waves.  Ties go to fewer slabs.
-int choose_slabs(int n_tiles, int total_kb, int grid) {
+int choose_slabs(int n_tiles, int total_kb, int kb_tokens, int grid) {
     const int smax = std::max(1, std::min(64, total_kb));
     int best = 1;
     double best_cost = 0.0;
     for (int S = 1; S <= smax; ++S) {
         const long long units = static_cast<long long>(n_tiles) * S;
         const long long waves = (units + grid - 1) / grid;
-        const double mma = 300.0 * std::ceil(static_cast<double>(total_kb) / S);
+        const double mma = 4.7 * kb_tokens * std::ceil(static_cast<double>(total_kb) / S);
         const double epi = S == 1 ? 12000.0 : 36000.0;
         const double cost = static_cast<double>(waves) * std::max(mma, epi);
         if (S == 1 || cost < best_cost * 0.98) {
@@ -260,7 +260,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         p.n_tiles = hk::pair_tile_count(h->T);
         const int pairs_max = h->grid > 0 ? std::max(1, h->grid / 2) : h->max_pairs;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
-                                   : choose_slabs(p.n_tiles, p.total_kb, pairs_max);
+                                   : choose_slabs(p.n_tiles, p.total_kb, hk::kKBlock, pairs_max);
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
         grid = 2 * std::min(pairs_max, p.n_units);
@@ -268,7 +268,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     } else {
         const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
-                                   : choose_slabs(h->n_tiles, p.total_kb, grid_max);
+                                   : choose_slabs(h->n_tiles, p.total_kb, kblock, grid_max);
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
         grid = std::min(grid_max, p.n_units);
@@ -361,7 +361,7 @@ HESS_EXPORT hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens
     if (!X) return fail(HESS_ERR_INVALID, "X is NULL with n_tokens > 0");
     if (reinterpret_cast<uintptr_t>(X) % 16 != 0) return fail(HESS_ERR_INVALID, "X is not 16-byte aligned");
     if (n_tokens > (int64_t(1) << 31) - hk::kKBlock)
-        return fail(HESS_ERR_UNSUPPORTED, "n_tokens exceeds 2^31 - 64 in one batch");
+        return fail(HESS_ERR_UNSUPPORTED, "n_tokens exceeds 2^31 - %d in one batch", hk::kKBlock);
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
@@ -483,7 +483,8 @@ HESS_EXPORT hess_status hess_set_option(hess_t h, int32_t option, int64_t value)
             return HESS_OK;
         case HESS_OPT_CHUNK_TOKENS:
             if (value < hk::kKBlock || value > 65536 || value % hk::kKBlock)
-                return fail(HESS_ERR_INVALID, "chunk_tokens must be a multiple of 64 in [64, 65536]");
+                return fail(HESS_ERR_INVALID, "chunk_tokens must be a multiple of %d in [%d, 65536]",
+                            hk::kKBlock, hk::kKBlock);
             h->chunk_tokens = static_cast<int>(value);
             return HESS_OK;
         case HESS_OPT_WAIT_TIMEOUT_NS:

@@ -11,8 +11,8 @@
 //   * one persistent CTA per SM walks a static list of units
 //     (tile, token slab); the token stream is the concatenation of the
 //     queued batches, so many small ragged batches form one split-K pass;
-//   * warp 0 stages X boxes of 64 tokens x 64 features with TMA
-//     (128-byte swizzle) into a 6-deep shared-memory ring; on diagonal
+//   * warp 0 stages X boxes of 128 tokens x 64 features with TMA
+//     (128-byte swizzle) into a 3-deep shared-memory ring; on diagonal
 //     tiles A and B are the same slab and are loaded once;
 //   * warp 1 issues tcgen05.mma (M=128, N=128, K=16, both operands
 //     MN-major straight from the row-major X boxes).  Consecutive 16-token
@@ -40,8 +40,8 @@ using syrk::unit_at;
 using syrk::kEpiWarps;
 using syrk::kDrainLimitNs;
 
-constexpr int kStages = 6;
-constexpr uint32_t kBoxBytes = 64 * 128;            // 64 tokens x 128 bytes
+constexpr int kStages = 3;
+constexpr uint32_t kBoxBytes = kKBlock * 128;       // kKBlock tokens x 128 bytes
 constexpr uint32_t kOperandBytes = 2 * kBoxBytes;   // 128 features
 constexpr uint32_t kStageBytes = 2 * kOperandBytes; // A and B
 constexpr int kThreads = (2 + kEpiWarps) * 32;
@@ -168,11 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                         const uint32_t sA = base + stage * kStageBytes;
                         const uint32_t sB = diag ? sA : sA + kOperandBytes;
 #pragma unroll
-                        for (int j = 0; j < kKBlock / 16; ++j) {
+                        for (int j = 0; j < kKSteps; ++j) {
                             const uint64_t ad = smem_desc_sw128(sA + j * 2048u, kBoxBytes, 1024u);
                             const uint64_t bd = smem_desc_sw128(sB + j * 2048u, kBoxBytes, 1024u);
                             // even steps -> bank 0, odd steps -> bank 1; each bank
-                            // starts afresh at the first step of the chunk
+                            // starts afresh at the first step of the chunk.  Rows
+                            // past a batch's end hold TMA's zeros and add nothing:
+                            // issuing them costs less than a per-stage test on
+                            // this thread's critical path (measured)
                             umma_f16(dt + (j & 1) * 128u, ad, bd, kIdesc,
                                      (kb > c0 || j > 1) ? 1u : 0u);
                         }

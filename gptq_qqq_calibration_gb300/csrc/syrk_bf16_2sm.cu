@@ -3,10 +3,10 @@
 //
 // Same sums as syrk_bf16.cu (GPTQModel PR #2979 Summary; NVIDIA
 // Model-Optimizer PR #3002, "What does this PR do?"), laid out for the
-// per-SM operand ingress that bounds the single-SM kernel (about 58 bytes per
-// clock per SM on GB300, measured): a pair computes a 256-row x 128-column
-// tile, each SM receiving its 128 rows of A and 64 of the 128 columns of B,
-// i.e. 24 KB per 64 tokens instead of 32 KB for the same tensor work.
+// per-SM operand feed that bounds the single-SM kernel: a pair computes a
+// 256-row x 128-column tile, each SM receiving its 128 rows of A and 64 of the
+// 128 columns of B, i.e. 48 KB per 128 tokens instead of 64 KB for the same
+// tensor work.
 //
 // Tiles: rows in blocks of 256 (I2), columns in blocks of 128 (J), J >= 2*I2
 // so that the upper triangle is covered.  CTA r of the pair owns rows
@@ -15,9 +15,9 @@
 // spans 256 rows) but not stored.
 //
 // Roles (both CTAs run all of them, except where noted):
-//   * warp 0: TMA producer for this CTA's A (2 boxes) and B (1 box), into an
-//     8-deep ring; the copies of both CTAs count their bytes on the even
-//     CTA's barrier (pair-mode TMA), which expects both;
+//   * warp 0: TMA producer for this CTA's A (2 boxes) and B (1 box) of 128
+//     tokens, into a 4-deep ring; the copies of both CTAs count their bytes
+//     on the even CTA's barrier (pair-mode TMA), which expects both;
 //   * warp 1 of the even CTA: issues tcgen05.mma.cta_group::2 (M=256, N=128,
 //     K=16), alternating 16-token steps between two accumulator banks, and
 //     multicasts every commit to both CTAs;
@@ -37,11 +37,11 @@ namespace {
 using syrk::kDrainLimitNs;
 using syrk::kEpiWarps;
 
-constexpr int kStages = 8;
-constexpr uint32_t kBoxBytes = 64 * 128;            // 64 tokens x 64 bf16
+constexpr int kStages = 4;
+constexpr uint32_t kBoxBytes = kKBlock * 128;       // kKBlock tokens x 64 bf16
 constexpr uint32_t kABytes = 2 * kBoxBytes;         // this CTA's 128 rows
 constexpr uint32_t kBBytes = kBoxBytes;             // this CTA's 64 columns
-constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 24 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 256, 128);
@@ -181,7 +181,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const uint32_t sA = base + stage * kStageBytes;
                         const uint32_t sB = sA + kABytes;
 #pragma unroll
-                        for (int j = 0; j < kKBlock / 16; ++j) {
+                        for (int j = 0; j < kKSteps; ++j) {
                             const uint64_t ad = smem_desc_sw128(sA + j * 2048u, kBoxBytes, 1024u);
                             // B is one 64-column slice per CTA: no second slice to
                             // stride to (a zero stride keeps any read inside it)

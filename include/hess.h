@@ -78,7 +78,7 @@ typedef enum {
     HESS_OPT_MAX_PENDING = 2,     /* pending batches that trigger a flush (1..192, default 192) */
     HESS_OPT_CHUNK_TOKENS = 3,    /* tokens per tensor-memory chunk before the compensated
                                      on-chip sum takes it; each chunk alternates 16-token
-                                     steps between two chains (64..65536, multiple of 64,
+                                     steps between two chains (128..65536, multiple of 128,
                                      default 256).  Tensor-core accumulation rounds toward
                                      zero, so longer chunks bias H low.  fp32 batches use
                                      chunks of an eighth of this (at least 32 tokens). */

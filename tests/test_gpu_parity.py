@@ -1,7 +1,7 @@
 """GPU parity of the CUDA path against the float64 oracle, small sizes.
 
 Every call goes through the C ABI (ctypes binding).  Sizes span several
-128x128 tiles, ragged token tails (n not a multiple of 64, n = 1), widths
+128x128 tiles, ragged token tails (n not a multiple of 128, n = 1), widths
 that are not multiples of the tile (136, 8), empty batches, several fused
 flushes, every split-K/chunk setting, and the degenerate N = 0 case.
 """
@@ -57,11 +57,11 @@ def test_bf16_matches_oracle(d, counts, pair):
 
 
 @pytest.mark.parametrize("opts", [
-    dict(chunk_tokens=64), dict(chunk_tokens=128, split_k=3), dict(split_k=7),
-    dict(grid=4), dict(grid=2, chunk_tokens=64), dict(flush_tokens=1),
+    dict(chunk_tokens=128), dict(chunk_tokens=384, split_k=3), dict(split_k=7),
+    dict(grid=4), dict(grid=2, chunk_tokens=128), dict(flush_tokens=1),
     dict(max_pending=3, chunk_tokens=4096), dict(split_k=40),
     dict(pair_kernel=0), dict(pair_kernel=0, split_k=3, grid=5),
-    dict(pair_kernel=0, grid=1, chunk_tokens=64), dict(pair_kernel=0, flush_tokens=1),
+    dict(pair_kernel=0, grid=1, chunk_tokens=384), dict(pair_kernel=0, flush_tokens=1),
 ])
 def test_bf16_schedules(opts):
     H, dv, Href, dref = _run(512, [700, 1, 64, 129, 512, 33], seed=11, **opts)
