@@ -273,6 +273,19 @@ __device__ __forceinline__ uint64_t two_sum2(uint64_t a, uint64_t b, uint64_t& e
     return s;
 }
 
+// ------------------------------------------------- register re-split
+
+// Every warp of a warpgroup executes the same one: .dec gives registers back
+// to the CTA's pool (the registers it was launched with), .inc takes them.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------ clusters / pairs
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -19,11 +19,13 @@
 //     steps alternate between two fp32 accumulator banks in tensor memory,
 //     and after `chunk_kb` k-blocks the pair is handed to the epilogue while
 //     the MMAs continue in a second pair (2 buffers x 2 banks x 128 columns);
-//   * warps 2-9 add the two banks and fold the chunk into a compensated
-//     (hi, lo) pair held in registers with an exact TwoSum on packed fp32
+//   * warps 4-11 add the two banks, sum the chunks into a `mid` pair of
+//     registers with round-to-nearest adds, and every 8 chunks fold mid
+//     into a compensated (hi, lo) pair with an exact TwoSum, on packed fp32
 //     pairs; at the end of a unit they add hi + lo in fp64 to the
 //     accumulator in global memory (red.add.f64, as several slabs may add
-//     to one tile).
+//     to one tile).  Warpgroup 0 (warps 0-3) gives registers to the
+//     epilogue warpgroups with setmaxnreg.
 // Why the short chains: tcgen05 accumulation into tensor memory rounds
 // toward zero, so a chain of k MMA steps loses about k ulps of its running
 // sum (measured on GB300: relative bias -1.8e-6 at 1,024 tokens, -2.6e-4 at
@@ -44,7 +46,17 @@ constexpr int kStages = 3;
 constexpr uint32_t kBoxBytes = kKBlock * 128;       // kKBlock tokens x 128 bytes
 constexpr uint32_t kOperandBytes = 2 * kBoxBytes;   // 128 features
 constexpr uint32_t kStageBytes = 2 * kOperandBytes; // A and B
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+// Warpgroup 0: warp 0 (producer), warp 1 (MMA issuer), warps 2-3 idle;
+// warpgroups 1-2: the epilogue.  The launch gives every thread kRegsLaunch
+// registers; warpgroup 0 hands most of its share to the epilogue's
+// (mid, hi, lo) fold state.
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;
+constexpr uint32_t kRegsLaunch = 168;  // 65536 / 384, rounded down to 8
+constexpr uint32_t kRegsLow = 56;
+constexpr uint32_t kRegsHigh = 224;
+static_assert(128 * kRegsLow + kEpiWarps * 32 * kRegsHigh <= kThreads * kRegsLaunch,
+              "register re-split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;  // [buffer][bank] x 128 columns
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 128, 128);
 constexpr int kNumBarriers = 2 * kStages + 5;
@@ -89,8 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const unsigned long long limit = p.timeout_ns;
-
-    if (warp == 0) {
+    if (warp < kFirstEpiWarp) {
+      setmaxnreg_dec<kRegsLow>();
+      if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             bool ok = true;
@@ -198,9 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             tc_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
+      }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
-        syrk::epilogue<kExcl>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+        setmaxnreg_inc<kRegsHigh>();
+        syrk::epilogue<kExcl, syrk::kMidGroup>(p, tmem, warp, lane, kFirstEpiWarp, accf_bar(0),
+                                               acce_bar(0), limit);
     }
 
     tc_fence_before();
@@ -226,7 +242,16 @@ cudaError_t syrk_bf16_prepare() {
     int blocks = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, syrk_bf16_kernel<false>, kThreads, kSmemBytes);
     if (e == cudaSuccess && blocks < 1) e = cudaErrorLaunchOutOfResources;
-    return e;
+    if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the CTA's pool has the registers: the pool
+    // must be what the re-split was sized for, or the epilogue would never start.
+    for (auto fn : {syrk_bf16_kernel<false>, syrk_bf16_kernel<true>}) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorLaunchOutOfResources;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s) {

@@ -21,7 +21,8 @@
 //   * warp 1 of the even CTA: issues tcgen05.mma.cta_group::2 (M=256, N=128,
 //     K=16), alternating 16-token steps between two accumulator banks, and
 //     multicasts every commit to both CTAs;
-//   * warps 2-9: the shared compensated epilogue on this CTA's 128 rows; they
+//   * warps 4-11: the shared compensated epilogue (chunk sums into `mid`,
+//     folded into (hi, lo) every 8 chunks) on this CTA's 128 rows; they
 //     release accumulator buffers on the even CTA's barrier (relaxed arrive:
 //     their tensor-memory loads have completed, and a release would wait for
 //     the unrelated fp64 reductions still in flight).
@@ -42,7 +43,16 @@ constexpr uint32_t kBoxBytes = kKBlock * 128;       // kKBlock tokens x 64 bf16
 constexpr uint32_t kABytes = 2 * kBoxBytes;         // this CTA's 128 rows
 constexpr uint32_t kBBytes = kBoxBytes;             // this CTA's 64 columns
 constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+// Warpgroup 0: warp 0 (producer), warp 1 (MMA issuer on the even CTA),
+// warps 2-3 idle; warpgroups 1-2: the epilogue, which takes most of
+// warpgroup 0's registers for its (mid, hi, lo) fold state.
+constexpr int kFirstEpiWarp = 4;
+constexpr int kThreads = (kFirstEpiWarp + kEpiWarps) * 32;
+constexpr uint32_t kRegsLaunch = 168;  // 65536 / 384, rounded down to 8
+constexpr uint32_t kRegsLow = 56;
+constexpr uint32_t kRegsHigh = 224;
+static_assert(128 * kRegsLow + kEpiWarps * 32 * kRegsHigh <= kThreads * kRegsLaunch,
+              "register re-split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 256, 128);
 constexpr int kNumBarriers = 2 * kStages + 5;
@@ -115,7 +125,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const unsigned long long limit = p.timeout_ns;
 
-    if (warp == 0) {
+    if (warp < kFirstEpiWarp) {
+      setmaxnreg_dec<kRegsLow>();
+      if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             bool ok = true;
@@ -211,12 +223,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_commit_pair_mc(drain_bar, 0x1);
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
+      }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
+        setmaxnreg_inc<kRegsHigh>();
         const int T = p.tiles_per_dim;
         const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-        syrk::epilogue_t<kExcl>(
-            p, tmem, warp, lane, 2, accf_bar(0), pair, n_pairs,
+        syrk::epilogue_t<kExcl, syrk::kMidGroup>(
+            p, tmem, warp, lane, kFirstEpiWarp, accf_bar(0), pair, n_pairs,
             [&](int u, int& k0, int& k1, int& out_tile) {
                 PairUnit un;
                 if (!pair_unit_at(p, u, un)) return false;
@@ -259,6 +273,14 @@ cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
         e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the CTA's pool has the registers: the pool
+    // must be what the re-split was sized for, or the epilogue would never start.
+    for (auto fn : {syrk_bf16_2sm_kernel<false>, syrk_bf16_2sm_kernel<true>}) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorLaunchOutOfResources;
+    }
     cudaLaunchConfig_t cfg = {};
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);

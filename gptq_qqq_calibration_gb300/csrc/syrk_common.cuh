@@ -32,22 +32,31 @@ __device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
 }
 
 constexpr int kEpiWarps = 8;                   // 2 per tensor-memory lane quarter
+constexpr int kMidGroup = 8;                   // chunks summed in `mid` between folds
 constexpr int kEpiCols = 4 * 128 / kEpiWarps;  // accumulator columns per warp
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
 // Epilogue of one CTA (kEpiWarps warps starting at first_warp).
 // Tensor memory holds 2 buffers x 2 banks x 128 columns; chunk c of a unit
 // sits in buffer (chunk counter & 1).  Each warp reads its lane quarter
-// (warp % 4) and kEpiCols of the 128 columns, adds the two banks, and folds the
-// sum into a (hi, lo) pair with Fast2Sum on packed fp32 pairs.  At the
-// end of a unit, hi + lo is added in fp64 to accumulator tile `out_tile`
-// (skipped when it is negative): by red.add.f64, or by a plain
+// (warp % 4) and kEpiCols of the 128 columns and adds the two banks, on
+// packed fp32 pairs.  The chunk sums reach a compensated (hi, lo) pair in
+// one of two ways:
+//   * kGroup == 0: every chunk sum is folded in with Fast2Sum;
+//   * kGroup > 0: chunk sums are added into `mid` with plain round-to-nearest
+//     adds (unbiased; over kGroup chunks their error is ~sqrt(kGroup) half-
+//     ulps of mid, i.e. ~1e-8 of the entry at the end of a long unit), and
+//     mid is folded in with an exact TwoSum every kGroup chunks and at the
+//     end of the unit.  This needs 3 x kEpiCols registers of state per
+//     thread (a re-split register budget) for about half the arithmetic.
+// At the end of a unit, hi + lo is added in fp64 to accumulator tile
+// `out_tile` (skipped when it is negative): by red.add.f64, or by a plain
 // read-modify-write when the launch has one token slab (kExcl, the kernel
 // instance chosen when p.exclusive is set).
 //   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
 //   wait_full(bar, parity) waits for a filled accumulator buffer;
 //   arrive_empty(b) releases buffer b to the MMA issuer.
-template <bool kExcl, class UnitFn, class WaitFn, class ArriveFn>
+template <bool kExcl, int kGroup, class UnitFn, class WaitFn, class ArriveFn>
 __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, int warp, int lane,
                                            int first_warp, uint32_t accf_bar0, int u0, int ustride,
                                            UnitFn unit_fn, WaitFn wait_full, ArriveFn arrive_empty) {
@@ -57,6 +66,7 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t col0 = static_cast<uint32_t>(part) * kEpiCols;
     uint64_t hi[kEpiCols / 2], lo[kEpiCols / 2];  // this thread's columns, as pairs
+    uint64_t mid[kGroup > 0 ? kEpiCols / 2 : 1];
     bool ok = true;
     int ab = 0;
     uint32_t aphase = 0;
@@ -64,6 +74,11 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         int k0, k1, out_tile;
         if (!unit_fn(u, k0, k1, out_tile)) continue;
         const int nch = (k1 - k0 + p.chunk_kb - 1) / p.chunk_kb;
+        if constexpr (kGroup > 0) {
+#pragma unroll
+            for (int i = 0; i < kEpiCols / 2; ++i) hi[i] = lo[i] = mid[i] = 0ull;
+        }
+        int g = 0;  // chunks in mid
         for (int c = 0; c < nch; ++c) {
             if (!wait_full(accf_bar0 + 8u * ab, aphase)) {
                 ok = false;
@@ -80,7 +95,9 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
                     const uint64_t v = add2(pack2(b0[2 * k], b0[2 * k + 1]),
                                             pack2(b1[2 * k], b1[2 * k + 1]));
                     const int i = it * 4 + k;
-                    if (c == 0) {
+                    if constexpr (kGroup > 0) {
+                        mid[i] = add2(mid[i], v);
+                    } else if (c == 0) {
                         hi[i] = v;
                         lo[i] = 0ull;
                     } else {
@@ -99,6 +116,19 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
             if (++ab == 2) {
                 ab = 0;
                 aphase ^= 1u;
+            }
+            if constexpr (kGroup > 0) {
+                // fold mid while the MMAs fill the other buffer
+                if (++g == kGroup || c + 1 == nch) {
+#pragma unroll
+                    for (int i = 0; i < kEpiCols / 2; ++i) {
+                        uint64_t e;
+                        hi[i] = two_sum2(hi[i], mid[i], e);
+                        lo[i] = add2(lo[i], e);
+                        mid[i] = 0ull;
+                    }
+                    g = 0;
+                }
             }
         }
         if (!ok) break;
@@ -139,11 +169,11 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
 }
 
 // The single-CTA form: units in blockIdx.x + k * gridDim.x order, local barriers.
-template <bool kExcl>
+template <bool kExcl, int kGroup>
 __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int warp, int lane,
                                          int first_warp, uint32_t accf_bar0, uint32_t acce_bar0,
                                          unsigned long long limit) {
-    epilogue_t<kExcl>(
+    epilogue_t<kExcl, kGroup>(
         p, tmem, warp, lane, first_warp, accf_bar0, blockIdx.x, gridDim.x,
         [&](int u, int& k0, int& k1, int& out_tile) {
             Unit un;

@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2-9)
-        syrk::epilogue<kExcl>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+        syrk::epilogue<kExcl, 0>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
     }
 
     tc_fence_before();
