@@ -139,7 +139,7 @@ struct hess_ctx {
     // options
     int64_t flush_tokens = 65536;
     int max_pending = hk::kMaxBatches;
-    int chunk_tokens = 256;
+    int chunk_tokens = 384;
     unsigned long long timeout_ns = 2000000000ull;
     int split_k = 0;
     int grid = 0;
