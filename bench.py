@@ -389,14 +389,14 @@ def _x_flush_per_call(hbm, bf16_burst):
     d = wl.d
     tri = d * (d + 1) // 2
     alg_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 4 * 2  # X once + fp32 upper-triangle RMW per call
-    acc_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 8 * 2  # what this library's fp64 tiles move
+    acc_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 8 * 2  # what this library's (hi, lo) tiles move
     out["flush_per_call"] = {
         "workload": wl.name + " (first 60 batches, one flush per batch)",
         "us_per_call": round(t / len(xs) * 1e6, 2), "tflops": round(algo_flops(wl.n_tokens, d) / t / 1e12, 2),
         "roofline": {"bound": "hbm", "achieved": round(alg_bytes / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(alg_bytes / t / 1e9 / hbm, 4),
                      "bytes_counted": "2*n*d + 8*d(d+1)/2 per call (X once, fp32 upper-triangle read+write)",
-                     "fp64_tile_bytes_per_s_GB": round(acc_bytes / t / 1e9, 1)}}
+                     "acc_tile_bytes_per_s_GB": round(acc_bytes / t / 1e9, 1)}}
     h.close()
     return out["flush_per_call"]
 
@@ -553,8 +553,8 @@ def _quantize_pass(d=4096, rows=4096, reps=3):
 
 
 def _x_merge(hbm, bf16_burst, d=4096, reps=5):
-    """hess_merge at d = 4,096: dst += src over the fp64 upper-triangle
-    tiles (69 MB each; 2 reads and 1 write per element)."""
+    """hess_merge at d = 4,096: dst += src over the (hi, lo) fp32 upper-
+    triangle tiles (69 MB each; 2 reads and 1 write per element)."""
     import torch
 
     from gptq_qqq_calibration_gb300 import Hessian
@@ -577,13 +577,13 @@ def _x_merge(hbm, bf16_burst, d=4096, reps=5):
         ts.append(e0.elapsed_time(e1) * 1e-3)
     t = statistics.median(ts)
     T = (d + 127) // 128
-    nbytes = 3 * T * (T + 1) // 2 * 128 * 128 * 8
+    nbytes = 3 * T * (T + 1) // 2 * 128 * 128 * 8  # 8 bytes per (hi, lo) element
     a.close()
     b.close()
-    return {"workload": f"hess_merge at d={d} (fp64 upper-triangle tiles)", "us_per_merge": round(t * 1e6, 2),
+    return {"workload": f"hess_merge at d={d} ((hi, lo) upper-triangle tiles)", "us_per_merge": round(t * 1e6, 2),
             "roofline": {"bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(nbytes / t / 1e9 / hbm, 4), "bytes_per_merge": nbytes,
-                         "kernel": "add_f64_kernel"}}
+                         "kernel": "add_pairs_kernel"}}
 
 
 EXTRAS = {

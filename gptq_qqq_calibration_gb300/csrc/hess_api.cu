@@ -117,7 +117,7 @@ struct hess_ctx {
     int T = 0;
     int n_tiles = 0;
     int sm_count = 0;
-    double* acc = nullptr;
+    float* acc = nullptr;  // (hi, lo) planes per upper tile
     uint32_t* status = nullptr;
     double* damp64 = nullptr;
     float* damp32 = nullptr;
@@ -326,7 +326,7 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     h->T = static_cast<int>(ceil_div(d, hk::kTile));
     h->n_tiles = h->T * (h->T + 1) / 2;
     cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
-    const size_t acc_bytes = static_cast<size_t>(h->n_tiles) * hk::kTileElems * sizeof(double);
+    const size_t acc_bytes = static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float);
     if (e == cudaSuccess) e = cudaMalloc(&h->acc, acc_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&h->status, 64);
     if (e == cudaSuccess) e = cudaMalloc(&h->damp64, sizeof(double));
@@ -463,7 +463,7 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->N = 0;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemsetAsync(h->acc, 0,
-                             static_cast<size_t>(h->n_tiles) * hk::kTileElems * sizeof(double), s));
+                             static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float), s));
     CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
     return mark_acc(h, s);
 }
@@ -548,9 +548,8 @@ HESS_EXPORT hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = flush_locked(src, s)) != HESS_OK) return st;
     if ((st = flush_locked(dst, s)) != HESS_OK) return st;
-    const size_t n = static_cast<size_t>(dst->n_tiles) * hk::kTileElems;
     if ((st = order_acc(src, s)) != HESS_OK || (st = order_acc(dst, s)) != HESS_OK) return st;
-    CUDA_TRY(hk::launch_add_f64(dst->acc, src->acc, n, dst->sm_count, s));
+    CUDA_TRY(hk::launch_add_pairs(dst->acc, src->acc, static_cast<size_t>(dst->n_tiles), dst->sm_count, s));
     if ((st = mark_acc(src, s)) != HESS_OK || (st = mark_acc(dst, s)) != HESS_OK) return st;
     dst->N += src->N;
     return HESS_OK;
@@ -572,7 +571,7 @@ HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream
     if (st != HESS_OK) return st;
     std::lock_guard<std::mutex> lk(src->mu);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = static_cast<size_t>(src->n_tiles) * hk::kTileElems * sizeof(double);
+    const size_t bytes = static_cast<size_t>(src->n_tiles) * hk::kTileWords * sizeof(float);
     if ((st = order_acc(src, s)) != HESS_OK) {
         hess_destroy(h);
         return st;

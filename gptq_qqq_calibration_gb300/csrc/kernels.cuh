@@ -9,10 +9,14 @@
 namespace hk {
 
 // Edge of a tile of H (features).  The accumulator holds the upper-triangle
-// tiles (I <= J), tile-major, each tile column-major: element (r, c) of tile
-// t is acc[t * kTile * kTile + c * kTile + r].
+// tiles (I <= J), tile-major.  Each element is an unevaluated sum hi + lo of
+// two fp32 values (about 48 significant bits), so that every update is fp32
+// arithmetic (GB300's fp64 pipe runs at ~1/64 of its fp32 rate).  A tile is a
+// plane of hi then a plane of lo, each column-major: element (r, c) of tile
+// t has hi at acc[t * kTileWords + c * kTile + r] and lo kTileElems further.
 constexpr int kTile = 128;
 constexpr int kTileElems = kTile * kTile;
+constexpr int kTileWords = 2 * kTileElems;
 // Tokens per pipeline stage ("k-block") of the bf16 SYRK kernels.  Larger
 // stages mean fewer barrier round trips per token between the TMA producer
 // and the MMA issuer; on GB300, 128-token stages (3 in flight) run 1.14x
@@ -53,8 +57,8 @@ struct SyrkParams {
     int32_t d;
     int32_t n_units;        // n_tiles * n_slabs
     int32_t exclusive;      // 1: one token slab, so each accumulator tile has one writer and the
-                            // epilogue reads, adds and stores it (else red.add.f64)
-    double* acc;            // fp64 accumulator (tile layout above)
+                            // epilogue reads, adds and stores it (else compensated atomics)
+    float* acc;             // (hi, lo) accumulator (tile layout above)
     uint32_t* status;
     unsigned long long timeout_ns;
 };
@@ -110,9 +114,9 @@ cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
 
 // Materialize: damp = damp_percent * mean_i(acc_ii * scale) into damp_out
 // (fp64) and damp_out_f32; then H_out (row-major d x d fp32).
-cudaError_t launch_diag_damp(const double* acc, int d, int T, double scale, double damp_percent,
+cudaError_t launch_diag_damp(const float* acc, int d, int T, double scale, double damp_percent,
                              double* damp_out, float* damp_out_f32, cudaStream_t s);
-cudaError_t launch_materialize(const double* acc, float* H_out, int d, int T, double scale,
+cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
                                const double* damp, cudaStream_t s);
 
 // Local 16x16 block Grams.
@@ -135,8 +139,9 @@ cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
                               cudaStream_t s);
 
-// dst += src over n fp64 elements (accumulator merge).
-cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_count, cudaStream_t s);
+// dst += src over n_tiles (hi, lo) accumulator tiles (accumulator merge).
+cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int sm_count,
+                             cudaStream_t s);
 // acc[i] += sum_t X[t][i]^2 (fp64 accumulator), X row-major [n, d], d % 8 == 0.
 cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
                             cudaStream_t s);

@@ -1,4 +1,4 @@
-// Materialize kernels: scale the fp64 accumulator by 2/N, add the damping
+// Materialize kernels: scale the (hi, lo) accumulator by 2/N, add the damping
 // term to the diagonal and write the full symmetric fp32 Hessian; and the
 // read-out of the local 16x16 block Hessians.
 //
@@ -9,8 +9,11 @@
 // GPTQModel PR #2979 Summary: N counts token vectors.
 //
 // Readings: the mean of the diagonal is taken of the scaled matrix, in
-// fp64; every output element is rounded once to fp32; H_out[j][i] is a copy
-// of H_out[i][j] (i <= j) so the result is exactly symmetric.
+// fp64; diagonal elements are computed in fp64 and rounded once to fp32;
+// off-diagonal elements (hi + lo) * scale are computed in fp32 with an exact
+// product (FMA) and rounded to within an ulp of the correctly rounded value;
+// H_out[j][i] is a copy of H_out[i][j] (i <= j) so the result is exactly
+// symmetric.
 #include "kernels.cuh"
 
 namespace hk {
@@ -18,7 +21,7 @@ namespace {
 
 constexpr int kDiagThreads = 1024;
 
-__global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const double* __restrict__ acc, int d,
+__global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const float* __restrict__ acc, int d,
                                                                  int T, double scale,
                                                                  double damp_percent,
                                                                  double* damp_out,
@@ -27,7 +30,8 @@ __global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const double* _
     double s = 0.0;
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         const int ti = i / kTile, r = i % kTile;
-        s += acc[static_cast<size_t>(tile_index(ti, ti, T)) * kTileElems + r * kTile + r];
+        const float* e = acc + static_cast<size_t>(tile_index(ti, ti, T)) * kTileWords + r * kTile + r;
+        s += static_cast<double>(e[0]) + static_cast<double>(e[kTileElems]);
     }
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
@@ -47,9 +51,10 @@ __global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const double* _
 // One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter in
 // its stored (column-major) order and writes the mirrored rows of H_out;
 // pass 2 writes the direct rows through a shared-memory transpose.
-__global__ void __launch_bounds__(256) materialize_kernel(const double* __restrict__ acc,
+__global__ void __launch_bounds__(256) materialize_kernel(const float* __restrict__ acc,
                                                           float* __restrict__ H, int d, int T,
-                                                          double scale,
+                                                          double scale, float scale_hi,
+                                                          float scale_lo,
                                                           const double* __restrict__ damp_ptr) {
     __shared__ float tr[64][65];
     const int t = blockIdx.x;
@@ -64,11 +69,22 @@ __global__ void __launch_bounds__(256) materialize_kernel(const double* __restri
     const double damp = *damp_ptr;
     const int r0 = I * kTile + a * 64, c0 = J * kTile + b * 64;
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-    const double* tile = acc + static_cast<size_t>(t) * kTileElems;
+    const float* tile = acc + static_cast<size_t>(t) * kTileWords;
     for (int cc = ty; cc < 64; cc += 4) {
         const int r = r0 + tx, c = c0 + cc;
-        const double s = tile[(b * 64 + cc) * kTile + a * 64 + tx];
-        const float v = (r == c) ? static_cast<float>(s * scale + damp) : static_cast<float>(s * scale);
+        const int k = (b * 64 + cc) * kTile + a * 64 + tx;
+        const float h = tile[k], l = tile[kTileElems + k];
+        float v;
+        if (r == c) {
+            v = static_cast<float>((static_cast<double>(h) + static_cast<double>(l)) * scale + damp);
+        } else {
+            // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
+            // as p + pe, plus the small cross terms, then one rounding
+            const float p = __fmul_rn(h, scale_hi);
+            const float pe = __fmaf_rn(h, scale_hi, -p);
+            const float cross = __fmaf_rn(l, scale_hi, __fmaf_rn(h, scale_lo, pe));
+            v = __fadd_rn(p, cross);
+        }
         tr[cc][tx] = v;
         if (r < d && c < d && r <= c) H[static_cast<size_t>(c) * d + r] = v;
     }
@@ -90,17 +106,20 @@ __global__ void __launch_bounds__(256) local_read_kernel(const double* __restric
 
 }  // namespace
 
-cudaError_t launch_diag_damp(const double* acc, int d, int T, double scale, double damp_percent,
+cudaError_t launch_diag_damp(const float* acc, int d, int T, double scale, double damp_percent,
                              double* damp_out, float* damp_out_f32, cudaStream_t s) {
     diag_damp_kernel<<<1, kDiagThreads, 0, s>>>(acc, d, T, scale, damp_percent, damp_out,
                                                 damp_out_f32);
     return cudaGetLastError();
 }
 
-cudaError_t launch_materialize(const double* acc, float* H_out, int d, int T, double scale,
+cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
                                const double* damp, cudaStream_t s) {
     const int n_tiles = T * (T + 1) / 2;
-    materialize_kernel<<<dim3(n_tiles, 4), 256, 0, s>>>(acc, H_out, d, T, scale, damp);
+    const float scale_hi = static_cast<float>(scale);
+    const float scale_lo = static_cast<float>(scale - static_cast<double>(scale_hi));
+    materialize_kernel<<<dim3(n_tiles, 4), 256, 0, s>>>(acc, H_out, d, T, scale, scale_hi, scale_lo,
+                                                        damp);
     return cudaGetLastError();
 }
 

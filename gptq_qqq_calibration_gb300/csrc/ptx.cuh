@@ -265,12 +265,25 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+// Scalar TwoSum: s + err == a + b exactly (no contraction into FMAs).
+__device__ __forceinline__ float two_sum_f32(float a, float b, float& err) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return s;
+}
+
 // Error-free transformation (TwoSum) on pairs: s + err == a + b exactly.
 __device__ __forceinline__ uint64_t two_sum2(uint64_t a, uint64_t b, uint64_t& err) {
     const uint64_t s = add2(a, b);
     const uint64_t bb = sub2(s, a);
     err = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
     return s;
+}
+
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------- register re-split
@@ -417,6 +430,16 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 
 __device__ __forceinline__ void red_add_f64(double* p, double v) {
     asm volatile("red.global.add.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+// Atomic fp32 add that returns the old value (the stored sum is old + v
+// rounded to nearest).
+__device__ __forceinline__ float atom_add_f32(float* p, float v) {
+    float old;
+    asm volatile("atom.global.add.f32 %0, [%1], %2;" : "=f"(old) : "l"(p), "f"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------- warp-level MMA

@@ -13,31 +13,49 @@
 namespace hk {
 namespace {
 
-// dst[i] += src[i] over n fp64 elements; 4 elements per thread, grid-stride.
-__global__ void __launch_bounds__(256) add_f64_kernel(double* __restrict__ dst,
-                                                      const double* __restrict__ src, size_t n) {
-    const size_t n4 = n / 4;
-    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
-        double4_32a a = reinterpret_cast<double4_32a*>(dst)[i];
-        const double4_32a b = reinterpret_cast<const double4_32a*>(src)[i];
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
-        reinterpret_cast<double4_32a*>(dst)[i] = a;
-    }
-    for (size_t i = n4 * 4 + blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-         i += stride)
-        dst[i] += src[i];
-}
-
 __device__ __forceinline__ float two_sum(float a, float b, float& err) {
     const float s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
     return s;
 }
+
+// dst += src over (hi, lo) accumulator tiles: per element, TwoSum of the hi
+// parts, the lo parts and the error added, and the pair renormalised with
+// Fast2Sum.  Four elements per thread (float4 of each plane), grid-stride
+// over the tiles' planes.
+__global__ void __launch_bounds__(256) add_pairs_kernel(float* __restrict__ dst,
+                                                        const float* __restrict__ src,
+                                                        size_t n_tiles) {
+    const size_t per_tile = kTileElems / 4;
+    const size_t n4 = n_tiles * per_tile;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t q = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; q < n4; q += stride) {
+        const size_t t = q / per_tile, k = (q - t * per_tile) * 4;
+        float* dh = dst + t * kTileWords + k;
+        const float* sh = src + t * kTileWords + k;
+        float4 ah = *reinterpret_cast<const float4*>(dh);
+        float4 al = *reinterpret_cast<const float4*>(dh + kTileElems);
+        const float4 bh = *reinterpret_cast<const float4*>(sh);
+        const float4 bl = *reinterpret_cast<const float4*>(sh + kTileElems);
+        float* const a_h[4] = {&ah.x, &ah.y, &ah.z, &ah.w};
+        float* const a_l[4] = {&al.x, &al.y, &al.z, &al.w};
+        const float b_h[4] = {bh.x, bh.y, bh.z, bh.w};
+        const float b_l[4] = {bl.x, bl.y, bl.z, bl.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float e;
+            const float s = two_sum(*a_h[i], b_h[i], e);
+            const float l = __fadd_rn(__fadd_rn(*a_l[i], b_l[i]), e);
+            const float hi = __fadd_rn(s, l);
+            *a_h[i] = hi;
+            *a_l[i] = __fsub_rn(l, __fsub_rn(hi, s));  // Fast2Sum error (|s| >= |l|)
+        }
+        *reinterpret_cast<float4*>(dh) = ah;
+        *reinterpret_cast<float4*>(dh + kTileElems) = al;
+    }
+}
+
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
@@ -118,10 +136,11 @@ __global__ void __launch_bounds__(256) colsumsq_read_kernel(const double* __rest
 
 }  // namespace
 
-cudaError_t launch_add_f64(double* dst, const double* src, size_t n, int sm_count, cudaStream_t s) {
-    const size_t want = (n / 4 + 255) / 256 + 1;
+cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int sm_count,
+                             cudaStream_t s) {
+    const size_t want = (n_tiles * (kTileElems / 4) + 255) / 256;
     const int grid = static_cast<int>(want < static_cast<size_t>(4 * sm_count) ? want : 4 * sm_count);
-    add_f64_kernel<<<grid, 256, 0, s>>>(dst, src, n);
+    add_pairs_kernel<<<grid, 256, 0, s>>>(dst, src, n_tiles);
     return cudaGetLastError();
 }
 

@@ -22,10 +22,10 @@
 //   * warps 4-11 add the two banks, sum the chunks into a `mid` pair of
 //     registers with round-to-nearest adds, and every 8 chunks fold mid
 //     into a compensated (hi, lo) pair with an exact TwoSum, on packed fp32
-//     pairs; at the end of a unit they add hi + lo in fp64 to the
-//     accumulator in global memory (red.add.f64, as several slabs may add
-//     to one tile).  Warpgroup 0 (warps 0-3) gives registers to the
-//     epilogue warpgroups with setmaxnreg.
+//     pairs; at the end of a unit they add (hi, lo) to the (hi, lo)
+//     accumulator tile in global memory with fp32 arithmetic (compensated
+//     atomics when several slabs add to one tile).  Warpgroup 0 (warps 0-3)
+//     gives registers to the epilogue warpgroups with setmaxnreg.
 // Why the short chains: tcgen05 accumulation into tensor memory rounds
 // toward zero, so a chain of k MMA steps loses about k ulps of its running
 // sum (measured on GB300: relative bias -1.8e-6 at 1,024 tokens, -2.6e-4 at

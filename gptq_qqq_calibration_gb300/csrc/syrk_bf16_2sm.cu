@@ -25,7 +25,7 @@
 //     folded into (hi, lo) every 8 chunks) on this CTA's 128 rows; they
 //     release accumulator buffers on the even CTA's barrier (relaxed arrive:
 //     their tensor-memory loads have completed, and a release would wait for
-//     the unrelated fp64 reductions still in flight).
+//     the unrelated accumulator atomics still in flight).
 // Every wait is bounded; both CTAs meet at a cluster barrier before tensor
 // memory is freed, so neither exits while the other still reads its memory.
 // After a timeout a CTA cannot watch its own copies land (they count on the

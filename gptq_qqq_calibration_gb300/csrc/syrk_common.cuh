@@ -49,10 +49,10 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 //     mid is folded in with an exact TwoSum every kGroup chunks and at the
 //     end of the unit.  This needs 3 x kEpiCols registers of state per
 //     thread (a re-split register budget) for about half the arithmetic.
-// At the end of a unit, hi + lo is added in fp64 to accumulator tile
-// `out_tile` (skipped when it is negative): by red.add.f64, or by a plain
-// read-modify-write when the launch has one token slab (kExcl, the kernel
-// instance chosen when p.exclusive is set).
+// At the end of a unit, (hi, lo) is added to the (hi, lo) accumulator tile
+// `out_tile` (skipped when it is negative): by a plain read-modify-write when
+// the launch has one token slab (kExcl, the kernel instance chosen when
+// p.exclusive is set), else by compensated fp32 atomics.
 //   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
 //   wait_full(bar, parity) waits for a filled accumulator buffer;
 //   arrive_empty(b) releases buffer b to the MMA issuer.
@@ -73,6 +73,12 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
     for (int u = u0; ok && u < p.n_units; u += ustride) {
         int k0, k1, out_tile;
         if (!unit_fn(u, k0, k1, out_tile)) continue;
+        if constexpr (kExcl) {
+            // the tile's old values travel to L2 while the unit's MMAs run
+            if (out_tile >= 0 && warp == first_warp && lane == 0)
+                prefetch_l2_bulk(p.acc + static_cast<size_t>(out_tile) * kTileWords,
+                                 kTileWords * sizeof(float));
+        }
         const int nch = (k1 - k0 + p.chunk_kb - 1) / p.chunk_kb;
         if constexpr (kGroup > 0) {
 #pragma unroll
@@ -133,35 +139,63 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         }
         if (!ok) break;
         if (out_tile < 0) continue;
-        double* const out = p.acc + static_cast<size_t>(out_tile) * kTileElems +
-                            static_cast<size_t>(col0) * kTile + row;
+        // this thread's row of hi; the lo plane is kTileElems further
+        float* const out = p.acc + static_cast<size_t>(out_tile) * kTileWords +
+                           static_cast<size_t>(col0) * kTile + row;
         if constexpr (kExcl) {
             // Sole writer of this tile in this launch: a plain read-modify-
-            // write, eight columns' loads in flight at a time.
+            // write of (hi, lo) += (hi', lo') with an exact TwoSum on the hi
+            // parts, kRmw columns' loads in flight at a time (with kGroup > 0
+            // the dead `mid` registers hold them).
+            constexpr int kRmw = kGroup > 0 ? 32 : 8;
 #pragma unroll
-            for (int g = 0; g < kEpiCols / 8; ++g) {
-                double old[8];
+            for (int g = 0; g < kEpiCols / kRmw; ++g) {
+                float oh[kRmw], ol[kRmw];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) old[i] = out[(8 * g + i) * kTile];
+                for (int i = 0; i < kRmw; ++i) {
+                    oh[i] = out[(kRmw * g + i) * kTile];
+                    ol[i] = out[kTileElems + (kRmw * g + i) * kTile];
+                }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < kRmw / 2; ++i) {
+                    uint64_t e;
+                    const uint64_t sh = two_sum2(pack2(__float_as_uint(oh[2 * i]), __float_as_uint(oh[2 * i + 1])),
+                                                 hi[kRmw / 2 * g + i], e);
+                    const uint64_t sl = add2(add2(pack2(__float_as_uint(ol[2 * i]), __float_as_uint(ol[2 * i + 1])),
+                                                  lo[kRmw / 2 * g + i]),
+                                             e);
                     float h0, h1, l0, l1;
-                    unpack2(hi[4 * g + i], h0, h1);
-                    unpack2(lo[4 * g + i], l0, l1);
-                    out[(8 * g + 2 * i) * kTile] =
-                        old[2 * i] + (static_cast<double>(h0) + static_cast<double>(l0));
-                    out[(8 * g + 2 * i + 1) * kTile] =
-                        old[2 * i + 1] + (static_cast<double>(h1) + static_cast<double>(l1));
+                    unpack2(sh, h0, h1);
+                    unpack2(sl, l0, l1);
+                    out[(kRmw * g + 2 * i) * kTile] = h0;
+                    out[(kRmw * g + 2 * i + 1) * kTile] = h1;
+                    out[kTileElems + (kRmw * g + 2 * i) * kTile] = l0;
+                    out[kTileElems + (kRmw * g + 2 * i + 1) * kTile] = l1;
                 }
             }
         } else {
+            // Several slabs add to this tile: an atomic add of hi' to hi
+            // returns the old value, from which the exact rounding error of
+            // that add is recovered (the stored sum is old + hi' rounded to
+            // nearest) and added, with lo', to lo.  Atomics go out in groups
+            // so that their round trips overlap.
+            constexpr int kAtom = 16;
 #pragma unroll
-            for (int i = 0; i < kEpiCols / 2; ++i) {
-                float h0, h1, l0, l1;
-                unpack2(hi[i], h0, h1);
-                unpack2(lo[i], l0, l1);
-                red_add_f64(out + (2 * i) * kTile, static_cast<double>(h0) + static_cast<double>(l0));
-                red_add_f64(out + (2 * i + 1) * kTile, static_cast<double>(h1) + static_cast<double>(l1));
+            for (int g = 0; g < kEpiCols / kAtom; ++g) {
+                float hv[kAtom], lv[kAtom], old[kAtom];
+#pragma unroll
+                for (int i = 0; i < kAtom / 2; ++i) {
+                    unpack2(hi[kAtom / 2 * g + i], hv[2 * i], hv[2 * i + 1]);
+                    unpack2(lo[kAtom / 2 * g + i], lv[2 * i], lv[2 * i + 1]);
+                }
+#pragma unroll
+                for (int i = 0; i < kAtom; ++i) old[i] = atom_add_f32(out + (kAtom * g + i) * kTile, hv[i]);
+#pragma unroll
+                for (int i = 0; i < kAtom; ++i) {
+                    float e;
+                    two_sum_f32(old[i], hv[i], e);
+                    red_add_f32(out + kTileElems + (kAtom * g + i) * kTile, __fadd_rn(lv[i], e));
+                }
             }
         }
     }

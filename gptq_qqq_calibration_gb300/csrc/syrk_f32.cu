@@ -20,7 +20,8 @@
 //     and the three small terms into bank 1, so they never ride on the
 //     large running sum;
 //   * warps 2-9 run the shared compensated epilogue (bank 0 + bank 1 folded
-//     into registers by TwoSum, fp64 add at the end of a unit).
+//     into registers by TwoSum, added to the (hi, lo) accumulator at the
+//     end of a unit).
 // Tensor-core accumulation rounds toward zero, so chunks are short (32
 // tokens by default: 4 hi*hi steps).  Every wait is bounded.
 #include "syrk_common.cuh"

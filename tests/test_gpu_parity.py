@@ -69,6 +69,39 @@ def test_bf16_schedules(opts):
     assert np.array_equal(H, H.T)
 
 
+@pytest.mark.parametrize("opts", [dict(split_k=1), dict(split_k=7), dict(split_k=40),
+                                  dict(split_k=1, pair_kernel=1), dict(split_k=40, pair_kernel=1),
+                                  dict(split_k=1, dtype=torch.float32), dict(split_k=40, dtype=torch.float32)])
+def test_accumulation_is_exact_on_integer_data(opts):
+    """Integer activations in [-64, 64] make every product and every
+    tensor-memory chain exact (chain sums stay below 2^24), so the only
+    rounding left is in the (hi, lo) accumulator, whose entries grow past
+    2^24.  The single-slab read-modify-write and the compensated atomics of
+    split-K launches must both keep the exact integer sum: H then equals the
+    oracle's exact sum times 2/N to within one fp32 ulp (a lost rounding
+    error of an fp32 add would show as an error of several ulps)."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    opts = dict(opts)
+    dtype = opts.pop("dtype", torch.bfloat16)
+    d, counts = 384, [6000, 5000, 3000]
+    h = Hessian(d, flush_tokens=1 << 20, **opts)
+    o = GramOracle(d)
+    g = torch.Generator(device="cuda").manual_seed(29)
+    for n in counts:
+        X = torch.randint(-64, 65, (n, d), generator=g, device="cuda").to(dtype)
+        h.add_batch(X)
+        o.add_batch(host(X))
+    H, _ = h.materialize(0.0)
+    h.sync()
+    H = H.cpu().numpy().astype(np.float64)
+    h.close()
+    Href, _ = o.materialize(0.0)
+    assert np.abs(o.S).max() > 2 ** 24  # the accumulator must round in fp32
+    ulp = np.spacing(np.abs(Href).astype(np.float32)).astype(np.float64)
+    err = np.abs(H - Href) / ulp
+    assert err.max() <= 1.0, f"max {err.max():.2f} ulp"
+
+
 @pytest.mark.parametrize("d,counts", [
     (256, [128, 128, 128, 128]),
     (136, [1, 31, 32, 33, 200]),
