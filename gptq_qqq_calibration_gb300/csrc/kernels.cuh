@@ -12,11 +12,14 @@ namespace hk {
 // tiles (I <= J), tile-major.  Each element is an unevaluated sum hi + lo of
 // two fp32 values (about 48 significant bits), so that every update is fp32
 // arithmetic (GB300's fp64 pipe runs at ~1/64 of its fp32 rate).  A tile is a
-// plane of hi then a plane of lo, each column-major: element (r, c) of tile
-// t has hi at acc[t * kTileWords + c * kTile + r] and lo kTileElems further.
+// plane of hi then a plane of lo.  A plane holds 4-column blocks: element
+// (r, c) sits at tile_offset(r, c), so that one thread moves 4 columns of its
+// row with a 16-byte access and a warp's 32 rows are 512 contiguous bytes.
+// The lo plane is kTileElems further.
 constexpr int kTile = 128;
 constexpr int kTileElems = kTile * kTile;
 constexpr int kTileWords = 2 * kTileElems;
+__host__ __device__ constexpr int tile_offset(int r, int c) { return ((c >> 2) * kTile + r) * 4 + (c & 3); }
 // Tokens per pipeline stage ("k-block") of the bf16 SYRK kernels.  Larger
 // stages mean fewer barrier round trips per token between the TMA producer
 // and the MMA issuer; on GB300, 128-token stages (3 in flight) run 1.14x

@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const float* __
     double s = 0.0;
     for (int i = threadIdx.x; i < d; i += blockDim.x) {
         const int ti = i / kTile, r = i % kTile;
-        const float* e = acc + static_cast<size_t>(tile_index(ti, ti, T)) * kTileWords + r * kTile + r;
+        const float* e = acc + static_cast<size_t>(tile_index(ti, ti, T)) * kTileWords + tile_offset(r, r);
         s += static_cast<double>(e[0]) + static_cast<double>(e[kTileElems]);
     }
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -48,9 +48,10 @@ __global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const float* __
     }
 }
 
-// One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter in
-// its stored (column-major) order and writes the mirrored rows of H_out;
-// pass 2 writes the direct rows through a shared-memory transpose.
+// One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter,
+// 4 columns of one row per thread (16-byte loads of each plane), and writes
+// the mirrored rows of H_out; pass 2 writes the direct rows through a
+// shared-memory transpose.
 __global__ void __launch_bounds__(256) materialize_kernel(const float* __restrict__ acc,
                                                           float* __restrict__ H, int d, int T,
                                                           double scale, float scale_hi,
@@ -70,23 +71,31 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
     const int r0 = I * kTile + a * 64, c0 = J * kTile + b * 64;
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
     const float* tile = acc + static_cast<size_t>(t) * kTileWords;
-    for (int cc = ty; cc < 64; cc += 4) {
-        const int r = r0 + tx, c = c0 + cc;
-        const int k = (b * 64 + cc) * kTile + a * 64 + tx;
-        const float h = tile[k], l = tile[kTileElems + k];
-        float v;
-        if (r == c) {
-            v = static_cast<float>((static_cast<double>(h) + static_cast<double>(l)) * scale + damp);
-        } else {
-            // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
-            // as p + pe, plus the small cross terms, then one rounding
-            const float p = __fmul_rn(h, scale_hi);
-            const float pe = __fmaf_rn(h, scale_hi, -p);
-            const float cross = __fmaf_rn(l, scale_hi, __fmaf_rn(h, scale_lo, pe));
-            v = __fadd_rn(p, cross);
+    for (int q = ty; q < 16; q += 4) {
+        const int k = tile_offset(a * 64 + tx, b * 64 + 4 * q);
+        const float4 h4 = *reinterpret_cast<const float4*>(tile + k);
+        const float4 l4 = *reinterpret_cast<const float4*>(tile + kTileElems + k);
+        const float hs[4] = {h4.x, h4.y, h4.z, h4.w};
+        const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+        const int r = r0 + tx;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int c = c0 + 4 * q + m;
+            const float h = hs[m], l = ls[m];
+            float v;
+            if (r == c) {
+                v = static_cast<float>((static_cast<double>(h) + static_cast<double>(l)) * scale + damp);
+            } else {
+                // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
+                // as p + pe, plus the small cross terms, then one rounding
+                const float p = __fmul_rn(h, scale_hi);
+                const float pe = __fmaf_rn(h, scale_hi, -p);
+                const float cross = __fmaf_rn(l, scale_hi, __fmaf_rn(h, scale_lo, pe));
+                v = __fadd_rn(p, cross);
+            }
+            tr[4 * q + m][tx] = v;
+            if (r < d && c < d && r <= c) H[static_cast<size_t>(c) * d + r] = v;
         }
-        tr[cc][tx] = v;
-        if (r < d && c < d && r <= c) H[static_cast<size_t>(c) * d + r] = v;
     }
     __syncthreads();
     for (int rr = ty; rr < 64; rr += 4) {

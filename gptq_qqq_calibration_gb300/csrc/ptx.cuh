@@ -441,6 +441,20 @@ __device__ __forceinline__ float atom_add_f32(float* p, float v) {
     asm volatile("atom.global.add.f32 %0, [%1], %2;" : "=f"(old) : "l"(p), "f"(v) : "memory");
     return old;
 }
+// The same on 4 consecutive floats (16-byte aligned), element-wise atomic.
+__device__ __forceinline__ float4 atom_add_v4_f32(float* p, float4 v) {
+    float4 o;
+    asm volatile("atom.global.add.v4.f32 {%0, %1, %2, %3}, [%4], {%5, %6, %7, %8};"
+                 : "=f"(o.x), "=f"(o.y), "=f"(o.z), "=f"(o.w)
+                 : "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+    return o;
+}
+__device__ __forceinline__ void red_add_v4_f32(float* p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 
 // ---------------------------------------------------------- warp-level MMA
 

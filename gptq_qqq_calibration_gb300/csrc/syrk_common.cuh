@@ -139,38 +139,39 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         }
         if (!ok) break;
         if (out_tile < 0) continue;
-        // this thread's row of hi; the lo plane is kTileElems further
-        float* const out = p.acc + static_cast<size_t>(out_tile) * kTileWords +
-                           static_cast<size_t>(col0) * kTile + row;
+        // this thread's row of the hi plane, from column col0 on (4-column
+        // blocks of 4 words); the lo plane is kTileElems further
+        float* const out = p.acc + static_cast<size_t>(out_tile) * kTileWords + tile_offset(row, col0);
         if constexpr (kExcl) {
             // Sole writer of this tile in this launch: a plain read-modify-
             // write of (hi, lo) += (hi', lo') with an exact TwoSum on the hi
-            // parts, kRmw columns' loads in flight at a time (with kGroup > 0
-            // the dead `mid` registers hold them).
+            // parts, 16-byte accesses, kRmw columns' loads in flight at a time
+            // (with kGroup > 0 the dead `mid` registers hold them).
             constexpr int kRmw = kGroup > 0 ? 32 : 8;
 #pragma unroll
             for (int g = 0; g < kEpiCols / kRmw; ++g) {
-                float oh[kRmw], ol[kRmw];
+                float4 oh[kRmw / 4], ol[kRmw / 4];
 #pragma unroll
-                for (int i = 0; i < kRmw; ++i) {
-                    oh[i] = out[(kRmw * g + i) * kTile];
-                    ol[i] = out[kTileElems + (kRmw * g + i) * kTile];
+                for (int i = 0; i < kRmw / 4; ++i) {
+                    const int q = (kRmw * g) / 4 + i;  // 4-column block of this thread
+                    oh[i] = *reinterpret_cast<const float4*>(out + q * 4 * kTile);
+                    ol[i] = *reinterpret_cast<const float4*>(out + kTileElems + q * 4 * kTile);
                 }
 #pragma unroll
-                for (int i = 0; i < kRmw / 2; ++i) {
-                    uint64_t e;
-                    const uint64_t sh = two_sum2(pack2(__float_as_uint(oh[2 * i]), __float_as_uint(oh[2 * i + 1])),
-                                                 hi[kRmw / 2 * g + i], e);
-                    const uint64_t sl = add2(add2(pack2(__float_as_uint(ol[2 * i]), __float_as_uint(ol[2 * i + 1])),
-                                                  lo[kRmw / 2 * g + i]),
-                                             e);
-                    float h0, h1, l0, l1;
-                    unpack2(sh, h0, h1);
-                    unpack2(sl, l0, l1);
-                    out[(kRmw * g + 2 * i) * kTile] = h0;
-                    out[(kRmw * g + 2 * i + 1) * kTile] = h1;
-                    out[kTileElems + (kRmw * g + 2 * i) * kTile] = l0;
-                    out[kTileElems + (kRmw * g + 2 * i + 1) * kTile] = l1;
+                for (int i = 0; i < kRmw / 4; ++i) {
+                    const int q = (kRmw * g) / 4 + i;
+                    uint64_t e0, e1;
+                    const uint64_t s0 = two_sum2(pack2(__float_as_uint(oh[i].x), __float_as_uint(oh[i].y)), hi[2 * q], e0);
+                    const uint64_t s1 = two_sum2(pack2(__float_as_uint(oh[i].z), __float_as_uint(oh[i].w)), hi[2 * q + 1], e1);
+                    const uint64_t t0 = add2(add2(pack2(__float_as_uint(ol[i].x), __float_as_uint(ol[i].y)), lo[2 * q]), e0);
+                    const uint64_t t1 = add2(add2(pack2(__float_as_uint(ol[i].z), __float_as_uint(ol[i].w)), lo[2 * q + 1]), e1);
+                    float4 nh, nl;
+                    unpack2(s0, nh.x, nh.y);
+                    unpack2(s1, nh.z, nh.w);
+                    unpack2(t0, nl.x, nl.y);
+                    unpack2(t1, nl.z, nl.w);
+                    *reinterpret_cast<float4*>(out + q * 4 * kTile) = nh;
+                    *reinterpret_cast<float4*>(out + kTileElems + q * 4 * kTile) = nl;
                 }
             }
         } else {
@@ -179,22 +180,34 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
             // that add is recovered (the stored sum is old + hi' rounded to
             // nearest) and added, with lo', to lo.  Atomics go out in groups
             // so that their round trips overlap.
-            constexpr int kAtom = 16;
+            constexpr int kAtomQ = 4;  // 4-column blocks per group
 #pragma unroll
-            for (int g = 0; g < kEpiCols / kAtom; ++g) {
-                float hv[kAtom], lv[kAtom], old[kAtom];
+            for (int g = 0; g < kEpiCols / (4 * kAtomQ); ++g) {
+                float4 hv[kAtomQ], lv[kAtomQ], old[kAtomQ];
 #pragma unroll
-                for (int i = 0; i < kAtom / 2; ++i) {
-                    unpack2(hi[kAtom / 2 * g + i], hv[2 * i], hv[2 * i + 1]);
-                    unpack2(lo[kAtom / 2 * g + i], lv[2 * i], lv[2 * i + 1]);
+                for (int i = 0; i < kAtomQ; ++i) {
+                    const int q = kAtomQ * g + i;
+                    unpack2(hi[2 * q], hv[i].x, hv[i].y);
+                    unpack2(hi[2 * q + 1], hv[i].z, hv[i].w);
+                    unpack2(lo[2 * q], lv[i].x, lv[i].y);
+                    unpack2(lo[2 * q + 1], lv[i].z, lv[i].w);
                 }
 #pragma unroll
-                for (int i = 0; i < kAtom; ++i) old[i] = atom_add_f32(out + (kAtom * g + i) * kTile, hv[i]);
+                for (int i = 0; i < kAtomQ; ++i)
+                    old[i] = atom_add_v4_f32(out + (kAtomQ * g + i) * 4 * kTile, hv[i]);
 #pragma unroll
-                for (int i = 0; i < kAtom; ++i) {
+                for (int i = 0; i < kAtomQ; ++i) {
                     float e;
-                    two_sum_f32(old[i], hv[i], e);
-                    red_add_f32(out + kTileElems + (kAtom * g + i) * kTile, __fadd_rn(lv[i], e));
+                    float4 l = lv[i];
+                    two_sum_f32(old[i].x, hv[i].x, e);
+                    l.x = __fadd_rn(l.x, e);
+                    two_sum_f32(old[i].y, hv[i].y, e);
+                    l.y = __fadd_rn(l.y, e);
+                    two_sum_f32(old[i].z, hv[i].z, e);
+                    l.z = __fadd_rn(l.z, e);
+                    two_sum_f32(old[i].w, hv[i].w, e);
+                    l.w = __fadd_rn(l.w, e);
+                    red_add_v4_f32(out + kTileElems + (kAtomQ * g + i) * 4 * kTile, l);
                 }
             }
         }
