@@ -26,6 +26,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Hessian-accum TFLOP/s & tokens/s at d=4096 (1 GB300); % of BF16/HBM roofline"
 
+# DRAM bytes (read + write) per SYRK launch of one step of the default workload, from an ncu
+# capture of the current kernel (profiles/syrk_bf16_d4096_ragged360_dram.md); set to None when
+# the kernel changes until it is captured again.
+SYRK_DRAM_BYTES_PER_LAUNCH = {"d4096_ragged360_loguniform": 1.752e9}
+
 
 def peaks():
     try:
@@ -188,7 +193,11 @@ def run_ours(args):
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (n_tok * d * 2 / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(syrk_tflops, 2), "peak": bf16_sust,
-                     "unit": "TFLOP/s", "frac": round(syrk_tflops / bf16_sust, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(syrk_tflops / bf16_sust, 4),
+                     "traffic": (SYRK_DRAM_BYTES_PER_LAUNCH.get(wl.name) if args.dtype == "bf16"
+                                 and not args.batches else None),
+                     "traffic_note": "ncu dram bytes per SYRK launch (profiles/); algorithmic X bytes "
+                                     "per launch %.3g" % (2.0 * n_tok * d / max(1, kern["launches"])),
                      "kernel": "syrk_%s_kernel" % args.dtype,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16, dense)",
                      "launches_timed": kern["launches"]},
