@@ -98,7 +98,10 @@ typedef enum {
 
 /* Create an accumulator for inputs of width d (features).  Allocates the
  * on-device accumulator once [P2: "allocate the partial buffer once"] on the
- * current device and zeroes it (synchronously).
+ * current device and zeroes it (synchronously).  The accumulator keeps each
+ * entry S[i][j] (i <= j) of the running Gram as an unevaluated sum of two
+ * fp32 values, about 48 significant bits: 4 * d * (d + 128) bytes
+ * (69 MB at d = 4096).
  *   d      : features, 1..32768; d % 8 == 0 is required (each token row must
  *            be a multiple of 16 bytes), else HESS_ERR_UNSUPPORTED.
  *   out    : receives the handle (host pointer, non-NULL).
@@ -130,10 +133,13 @@ hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens, int32_t dt
 hess_status hess_flush(hess_t h, hess_stream_t stream);
 
 /* Flush, then write the damped Hessian [P4]:
- *     H_out[i][j] = H_out[j][i] = fp32(S[i][j] * (2/N))          (i <= j)
+ *     H_out[i][j] = H_out[j][i] = fp32(S[i][j] * (2/N))          (i < j)
  *     H_out[i][i] = fp32(S[i][i] * (2/N) + damp),
  *     damp        = damp_percent * mean_i(S[i][i] * (2/N))        (fp64)
- * H_out is bit-exactly symmetric.  With N == 0 it is all zeros and damp = 0.
+ * Diagonal entries are rounded once from fp64; off-diagonal entries come
+ * within one ulp of the correctly rounded value (fp32 arithmetic with an
+ * exact product).  H_out is bit-exactly symmetric.  With N == 0 it is all
+ * zeros and damp = 0.
  *   H_out          : device pointer, row-major [d, d] fp32, 16-byte aligned.
  *   damp_percent   : in [0, 1).  (QQQ validates (0,1) and defaults to 0.005;
  *                    0 returns the undamped H.)
