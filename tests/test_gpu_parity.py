@@ -277,6 +277,21 @@ def test_invalid_pointer_alignment_is_rejected():
     hess_destroy(h)
 
 
+def test_chunk_option_is_whole_pipeline_stages():
+    """bf16 chunks are whole 128-token pipeline stages: other lengths are
+    rejected before any launch, and the handle stays usable."""
+    from gptq_qqq_calibration_gb300 import Hessian, HessError
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_INVALID
+    h = Hessian(256)
+    for bad in (0, 64, 200, 65536 + 128):
+        with pytest.raises(HessError) as ei:
+            h.set_option("chunk_tokens", bad)
+        assert ei.value.status == HESS_ERR_INVALID
+    for good in (128, 384, 65536):
+        h.set_option("chunk_tokens", good)
+    h.close()
+
+
 def test_device_wait_limit_reports_timeout_and_handle_recovers():
     """A zero wait limit makes the kernel's first unsatisfied wait give up;
     the kernel drains its copies, frees tensor memory and returns, and the
