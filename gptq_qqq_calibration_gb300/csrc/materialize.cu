@@ -49,9 +49,12 @@ __global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const float* __
 }
 
 // One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter,
-// 4 columns of one row per thread (16-byte loads of each plane), and writes
-// the mirrored rows of H_out; pass 2 writes the direct rows through a
-// shared-memory transpose.
+// 4 columns of one row per thread (16-byte loads of each plane), computes
+// (hi + lo) * 2/N in fp32 and writes the mirrored strictly-upper rows of
+// H_out; a diagonal quarter then recomputes its diagonal in fp64 with the
+// damping (kept out of the main loop, where a per-element branch would put
+// fp64 work on every element); pass 2 writes the direct rows, diagonal
+// included, through the shared-memory transpose.
 __global__ void __launch_bounds__(256) materialize_kernel(const float* __restrict__ acc,
                                                           float* __restrict__ H, int d, int T,
                                                           double scale, float scale_hi,
@@ -67,40 +70,41 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
     }
     const int J = I + rem;
     if (I == J && a > b) return;  // lower quarter of a diagonal tile: covered by its mirror
-    const double damp = *damp_ptr;
     const int r0 = I * kTile + a * 64, c0 = J * kTile + b * 64;
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
     const float* tile = acc + static_cast<size_t>(t) * kTileWords;
+    const int r = r0 + tx;
     for (int q = ty; q < 16; q += 4) {
         const int k = tile_offset(a * 64 + tx, b * 64 + 4 * q);
         const float4 h4 = *reinterpret_cast<const float4*>(tile + k);
         const float4 l4 = *reinterpret_cast<const float4*>(tile + kTileElems + k);
         const float hs[4] = {h4.x, h4.y, h4.z, h4.w};
         const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
-        const int r = r0 + tx;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int c = c0 + 4 * q + m;
-            const float h = hs[m], l = ls[m];
-            float v;
-            if (r == c) {
-                v = static_cast<float>((static_cast<double>(h) + static_cast<double>(l)) * scale + damp);
-            } else {
-                // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
-                // as p + pe, plus the small cross terms, then one rounding
-                const float p = __fmul_rn(h, scale_hi);
-                const float pe = __fmaf_rn(h, scale_hi, -p);
-                const float cross = __fmaf_rn(l, scale_hi, __fmaf_rn(h, scale_lo, pe));
-                v = __fadd_rn(p, cross);
-            }
+            // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
+            // as p + pe, plus the small cross terms, then one rounding
+            const float p = __fmul_rn(hs[m], scale_hi);
+            const float pe = __fmaf_rn(hs[m], scale_hi, -p);
+            const float cross = __fmaf_rn(ls[m], scale_hi, __fmaf_rn(hs[m], scale_lo, pe));
+            const float v = __fadd_rn(p, cross);
             tr[4 * q + m][tx] = v;
-            if (r < d && c < d && r <= c) H[static_cast<size_t>(c) * d + r] = v;
+            if (r < c && c < d) H[static_cast<size_t>(c) * d + r] = v;
         }
     }
     __syncthreads();
+    if (I == J && a == b) {
+        if (ty == 0 && r < d) {
+            const int k = tile_offset(a * 64 + tx, a * 64 + tx);
+            const double s = static_cast<double>(tile[k]) + static_cast<double>(tile[kTileElems + k]);
+            tr[tx][tx] = static_cast<float>(s * scale + *damp_ptr);
+        }
+        __syncthreads();
+    }
     for (int rr = ty; rr < 64; rr += 4) {
-        const int r = r0 + rr, c = c0 + tx;
-        if (r < d && c < d && r <= c) H[static_cast<size_t>(r) * d + c] = tr[tx][rr];
+        const int r2 = r0 + rr, c = c0 + tx;
+        if (r2 < d && c < d && r2 <= c) H[static_cast<size_t>(r2) * d + c] = tr[tx][rr];
     }
 }
 
