@@ -38,6 +38,9 @@ PROTOTYPES = {
     "hess_destroy": (_i32, [_vp]),
     "hess_merge": (_i32, [_vp, _vp, _vp]),
     "hess_clone": (_i32, [_vp, ctypes.POINTER(_vp), _vp]),
+    "hess_state_bytes": (_i64, [_vp]),
+    "hess_export_state": (_i32, [_vp, _vp, _i64, _vp, ctypes.POINTER(_i64)]),
+    "hess_import_state": (_i32, [_vp, _vp, _i64, _i64, _vp]),
     "imatrix_create": (_i32, [_i64, ctypes.POINTER(_vp)]),
     "imatrix_add": (_i32, [_vp, _vp, _i64, _i32, _vp]),
     "imatrix_read": (_i32, [_vp, _vp, _vp]),

@@ -597,6 +597,56 @@ HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream
     return HESS_OK;
 }
 
+// ------------------------------------------------------ checkpoint / resume
+
+HESS_EXPORT int64_t hess_state_bytes(hess_t h) {
+    if (!h) return 0;
+    return static_cast<int64_t>(h->n_tiles) * hk::kTileWords * static_cast<int64_t>(sizeof(float));
+}
+
+HESS_EXPORT hess_status hess_export_state(hess_t h, void* dst, int64_t bytes, hess_stream_t stream,
+                                          int64_t* n_tokens_out) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (!dst || !n_tokens_out) return fail(HESS_ERR_INVALID, "dst or n_tokens_out is NULL");
+    const int64_t need = hess_state_bytes(h);
+    if (bytes < need)
+        return fail(HESS_ERR_INVALID, "state needs %lld bytes, got %lld", static_cast<long long>(need),
+                    static_cast<long long>(bytes));
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = flush_locked(h, s)) != HESS_OK) return st;
+    if ((st = order_acc(h, s)) != HESS_OK) return st;
+    CUDA_TRY(cudaMemcpyAsync(dst, h->acc, static_cast<size_t>(need), cudaMemcpyDefault, s));
+    if ((st = mark_acc(h, s)) != HESS_OK) return st;
+    *n_tokens_out = h->N;
+    return HESS_OK;
+}
+
+HESS_EXPORT hess_status hess_import_state(hess_t h, const void* src, int64_t bytes, int64_t n_tokens,
+                                          hess_stream_t stream) {
+    if (!h) return fail(HESS_ERR_INVALID, "handle is NULL");
+    if (!src) return fail(HESS_ERR_INVALID, "src is NULL");
+    if (n_tokens < 0) return fail(HESS_ERR_INVALID, "n_tokens < 0");
+    const int64_t need = hess_state_bytes(h);
+    if (bytes != need)
+        return fail(HESS_ERR_INVALID, "state of %lld bytes for a handle that holds %lld",
+                    static_cast<long long>(bytes), static_cast<long long>(need));
+    std::lock_guard<std::mutex> lk(h->mu);
+    hess_status st = check_device(h->device);
+    if (st != HESS_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->pending.clear();
+    h->pending_tokens = 0;
+    h->pending_dtype = -1;
+    if ((st = order_acc(h, s)) != HESS_OK) return st;
+    CUDA_TRY(cudaMemcpyAsync(h->acc, src, static_cast<size_t>(need), cudaMemcpyDefault, s));
+    CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
+    h->N = n_tokens;
+    return mark_acc(h, s);
+}
+
 // ----------------------------------------------------------- imatrix (f3)
 
 struct imatrix_ctx {

@@ -25,7 +25,8 @@ __all__ = [
     "hess_pending_batches", "hess_sync", "hess_reset", "hess_set_option", "hess_destroy",
     "local_hess_create", "local_hess_add", "local_hess_read", "local_hess_token_count",
     "local_hess_sync", "local_hess_reset", "local_hess_destroy",
-    "hess_merge", "hess_clone", "imatrix_create", "imatrix_add", "imatrix_read",
+    "hess_merge", "hess_clone", "hess_state_bytes", "hess_export_state", "hess_import_state",
+    "imatrix_create", "imatrix_add", "imatrix_read",
     "imatrix_token_count", "imatrix_reset", "imatrix_destroy",
     "Hessian", "LocalHessian", "IMatrix",
 ]
@@ -110,6 +111,24 @@ def hess_clone(src: int, stream=None) -> int:
     h = ctypes.c_void_p()
     check(_lib.load().hess_clone(src, ctypes.byref(h), _stream(stream)))
     return h.value
+
+
+def hess_state_bytes(h: int) -> int:
+    return int(_lib.load().hess_state_bytes(h))
+
+
+def hess_export_state(h: int, dst: torch.Tensor, stream=None) -> int:
+    """Copy the state into `dst` (a contiguous uint8 tensor on the host or the
+    device); returns the token count N."""
+    n = ctypes.c_int64()
+    check(_lib.load().hess_export_state(h, dst.data_ptr(), dst.numel() * dst.element_size(),
+                                        _stream(stream), ctypes.byref(n)))
+    return n.value
+
+
+def hess_import_state(h: int, src: torch.Tensor, n_tokens: int, stream=None) -> None:
+    check(_lib.load().hess_import_state(h, src.data_ptr(), src.numel() * src.element_size(),
+                                        int(n_tokens), _stream(stream)))
 
 
 def imatrix_create(d: int) -> int:
@@ -242,6 +261,24 @@ class Hessian:
         h._queued = []
         self._release()
         return h
+
+    def export_state(self, device: str = "cpu", stream=None) -> tuple:
+        """A checkpoint: (state, N), the state a uint8 tensor on `device` (host
+        memory is pinned).  The copy has completed when this returns."""
+        buf = torch.empty(hess_state_bytes(self.handle), dtype=torch.uint8, device=device)
+        if buf.device.type == "cpu":
+            buf = buf.pin_memory()
+        n = hess_export_state(self.handle, buf, stream)
+        hess_sync(self.handle, stream)
+        self._release()
+        return buf, n
+
+    def import_state(self, state: torch.Tensor, n_tokens: int, stream=None) -> None:
+        """Resume from a checkpoint of export_state (queued batches are dropped)."""
+        state = state.contiguous()
+        hess_import_state(self.handle, state, n_tokens, stream)
+        self._queued = []
+        hess_sync(self.handle, stream)
 
     def close(self) -> None:
         if self.handle:

@@ -186,6 +186,29 @@ hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream);
  * Allocates like hess_create; the copy is enqueued on `stream`. */
 hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream);
 
+/* Checkpoint and resume.  The pages checkpoint only the quantized model; a
+ * long calibration run also wants to save its partial Gram and token count
+ * and resume later, so these calls have no counterpart on the pages.
+ * The state is the accumulator in the library's own layout: an opaque blob of
+ * hess_state_bytes(h) bytes, valid for a handle of the same width d and a
+ * library of the same HESS_ABI_VERSION. */
+int64_t hess_state_bytes(hess_t h);  /* 0 for a NULL handle */
+
+/* Flush, then copy the state to `dst` (host or device memory, `bytes` >=
+ * hess_state_bytes(h)) on `stream`, and store the token count N in
+ * *n_tokens_out (host pointer, non-NULL).  With pageable host memory the copy
+ * is synchronous; otherwise the caller synchronises `stream` before reading
+ * dst.  Errors: INVALID (NULL, bytes too small), CUDA. */
+hess_status hess_export_state(hess_t h, void* dst, int64_t bytes, hess_stream_t stream,
+                              int64_t* n_tokens_out);
+
+/* Replace the handle's state by a blob from hess_export_state and set N to
+ * n_tokens.  Batches still queued are dropped (as by hess_reset); `src` is
+ * read on `stream`.  Errors: INVALID (NULL, bytes != hess_state_bytes(h),
+ * n_tokens < 0), CUDA. */
+hess_status hess_import_state(hess_t h, const void* src, int64_t bytes, int64_t n_tokens,
+                              hess_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* imatrix statistic [P3: "a per-column sum of squares, not a GEMM"]        */
 

@@ -1,6 +1,6 @@
 """GPU tests of the companion statistics: merging partial accumulators,
-cloning a Hessian (shared-input dedup), and the imatrix column sums of
-squares, each against the float64 oracle."""
+cloning a Hessian (shared-input dedup), checkpoint and resume, and the
+imatrix column sums of squares, each against the float64 oracle."""
 
 import numpy as np
 import pytest
@@ -87,6 +87,62 @@ def test_clone_is_an_independent_copy():
     assert rel_err(H2.cpu().numpy(), o.hessian()) <= TOL_BF16
     leader.close()
     follower.close()
+
+
+@pytest.mark.parametrize("where", ["cpu", "cuda"])
+def test_checkpoint_resume_equals_an_uninterrupted_run(where):
+    """A run exported after part A and resumed in a fresh handle gives, after
+    part B, exactly the H of one handle that ran A then B with the same
+    flushes; and both match the oracle."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    d = 384
+    a_counts, b_counts = [700, 129, 1], [513, 64]
+    xa = list(batches(d, a_counts, 31, "outlier"))
+    xb = list(batches(d, b_counts, 32, "outlier"))
+    ref = Hessian(d)
+    for X in xa:
+        ref.add_batch(X)
+    ref.flush()
+    for X in xb:
+        ref.add_batch(X)
+    H_ref, _ = ref.materialize(0.01)
+
+    first = Hessian(d)
+    for X in xa:
+        first.add_batch(X)
+    state, n = first.export_state(device=where)
+    first.close()
+    assert n == sum(a_counts)
+    resumed = Hessian(d)
+    resumed.add_batch(xb[0])  # dropped by the import
+    resumed.import_state(state, n)
+    assert resumed.n_tokens == n
+    for X in xb:
+        resumed.add_batch(X)
+    H, _ = resumed.materialize(0.01)
+    torch.cuda.synchronize()
+    assert torch.equal(H, H_ref)
+    o = GramOracle(d)
+    for X in xa + xb:
+        o.add_batch(host(X))
+    Href, _ = o.materialize(0.01)
+    assert rel_err(H.cpu().numpy(), Href) <= TOL_BF16
+    ref.close()
+    resumed.close()
+
+
+def test_import_rejects_a_state_of_another_width():
+    from gptq_qqq_calibration_gb300 import Hessian, HessError
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_INVALID
+    small, big = Hessian(256), Hessian(384)
+    state, n = small.export_state()
+    with pytest.raises(HessError) as ei:
+        big.import_state(state, n)
+    assert ei.value.status == HESS_ERR_INVALID
+    with pytest.raises(HessError):
+        small.import_state(state, -1)
+    small.close()
+    big.close()
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
