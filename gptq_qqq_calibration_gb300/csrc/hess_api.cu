@@ -173,12 +173,11 @@ hess_status check_device(int dev) {
 
 // Split-K factor (token slabs) from a per-unit cost model in SM cycles:
 // each unit costs max(MMA, epilogue), waves of units run back to back.  The
-// MMA part is ~4.7 cycles per token of a 128 x 128 tile; the
-// epilogue moves a 128 KB fp64 tile: ~12k cycles as a plain read-modify-
-// write (one slab, one writer per tile, HBM-bound) and ~36k with
-// red.add.f64 (several slabs; L2 applies fp64 adds at ~1.1 TB/s).  Small
-// flushes are epilogue-bound and take one slab; large ones split to fill
-// the waves.  Ties go to fewer slabs.
+// MMA part is ~4.7 cycles per token of a 128 x 128 tile; the epilogue writes
+// a 128 KB (hi, lo) tile back: a plain read-modify-write with one slab (one
+// writer per tile), compensated atomics with several, which cost about three
+// times as much.  Small flushes are epilogue-bound and take one slab; large
+// ones split to fill the waves.  Ties go to fewer slabs.
 int choose_slabs(int n_tiles, int total_kb, int kb_tokens, int grid) {
     const int smax = std::max(1, std::min(64, total_kb));
     int best = 1;
