@@ -119,7 +119,7 @@ struct hess_ctx {
     int sm_count = 0;
     float* acc = nullptr;  // (hi, lo) planes per upper tile
     uint32_t* status = nullptr;
-    double* damp64 = nullptr;
+    double* damp64 = nullptr;  // the damping value, then materialize's scratch
     float* damp32 = nullptr;
     cudaEvent_t ev = nullptr;
     // The accumulator's last user: work on another stream waits for it
@@ -328,9 +328,10 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     const size_t acc_bytes = static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float);
     if (e == cudaSuccess) e = cudaMalloc(&h->acc, acc_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&h->status, 64);
-    if (e == cudaSuccess) e = cudaMalloc(&h->damp64, sizeof(double));
+    if (e == cudaSuccess) e = cudaMalloc(&h->damp64, hk::materialize_scratch_bytes(h->T));
     if (e == cudaSuccess) e = cudaMalloc(&h->damp32, sizeof(float));
     if (e == cudaSuccess) e = cudaMemset(h->acc, 0, acc_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->damp64, 0, hk::materialize_scratch_bytes(h->T));
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_acc, cudaEventDisableTiming);
@@ -414,9 +415,8 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
     }
     const double scale = 2.0 / static_cast<double>(h->N);
     if ((st = order_acc(h, s)) != HESS_OK) return st;
-    CUDA_TRY(hk::launch_diag_damp(h->acc, static_cast<int>(h->d), h->T, scale, damp_percent,
-                                  h->damp64, h->damp32, s));
-    CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, h->damp64, s));
+    CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, damp_percent,
+                                    h->damp64, h->damp32, s));
     if ((st = mark_acc(h, s)) != HESS_OK) return st;
     if (damp_value_out) {
         float v = 0.0f;

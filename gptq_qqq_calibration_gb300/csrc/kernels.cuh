@@ -117,10 +117,11 @@ cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
 
 // Materialize: damp = damp_percent * mean_i(acc_ii * scale) into damp_out
 // (fp64) and damp_out_f32; then H_out (row-major d x d fp32).
-cudaError_t launch_diag_damp(const float* acc, int d, int T, double scale, double damp_percent,
-                             double* damp_out, float* damp_out_f32, cudaStream_t s);
+// Scratch of one materialization: the fp64 damping value, per-quarter sums
+// of the diagonal and an arrival count (zeroed once, left zero by each launch).
+size_t materialize_scratch_bytes(int T);
 cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
-                               const double* damp, cudaStream_t s);
+                               double damp_percent, double* scratch, float* damp_f32, cudaStream_t s);
 
 // Local 16x16 block Grams.
 constexpr int kLocalKBlock = 64;   // tokens per stage

@@ -19,67 +19,65 @@
 namespace hk {
 namespace {
 
-constexpr int kDiagThreads = 1024;
+// Scratch words of one materialization (device memory of the handle):
+// [0] the damping value (fp64), [1, 1 + 2T) the fp64 sums of the diagonal
+// quarters, then a 32-bit arrival count of those quarters, zero between
+// launches.
+__host__ __device__ constexpr size_t ticket_offset(int T) { return sizeof(double) * (1 + 2 * static_cast<size_t>(T)); }
 
-__global__ void __launch_bounds__(kDiagThreads) diag_damp_kernel(const float* __restrict__ acc, int d,
-                                                                 int T, double scale,
-                                                                 double damp_percent,
-                                                                 double* damp_out,
-                                                                 float* damp_out_f32) {
-    __shared__ double part[kDiagThreads / 32];
-    double s = 0.0;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        const int ti = i / kTile, r = i % kTile;
-        const float* e = acc + static_cast<size_t>(tile_index(ti, ti, T)) * kTileWords + tile_offset(r, r);
-        s += static_cast<double>(e[0]) + static_cast<double>(e[kTileElems]);
-    }
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        s = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.0;
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (threadIdx.x == 0) {
-            const double mean = (s * scale) / static_cast<double>(d);
-            const double damp = damp_percent * mean;
-            *damp_out = damp;
-            *damp_out_f32 = static_cast<float>(damp);
-        }
-    }
-}
-
-// One CTA per 64x64 quarter of an upper tile.  Pass 1 reads the quarter,
-// 4 columns of one row per thread (16-byte loads of each plane), computes
-// (hi + lo) * 2/N in fp32 and writes the mirrored strictly-upper rows of
-// H_out; a diagonal quarter then recomputes its diagonal in fp64 with the
-// damping (kept out of the main loop, where a per-element branch would put
-// fp64 work on every element); pass 2 writes the direct rows, diagonal
-// included, through the shared-memory transpose.
+// One CTA per 64x64 quarter of an upper tile, the diagonal tiles' quarters
+// first (so that the diagonal tail below overlaps the rest); blockIdx.x =
+// 4 * (tile in that order) + quarter.  Each thread loads all of its
+// 16-byte words of both planes first (4 columns of one row per word),
+// computes (hi + lo) * 2/N in fp32 and writes the mirrored strictly-upper
+// rows of H_out; pass 2 writes the direct strictly-upper rows through the
+// shared-memory transpose.  Diagonal elements are left to the tail: each
+// diagonal quarter stores the fp64 sum of its 64 diagonal (hi + lo), and the
+// last of them to arrive takes the mean of the scaled diagonal (its partial
+// sums added in a fixed order), writes the damping value and every diagonal
+// element, rounded once from fp64, while other quarters may still run.
 __global__ void __launch_bounds__(256) materialize_kernel(const float* __restrict__ acc,
                                                           float* __restrict__ H, int d, int T,
                                                           double scale, float scale_hi,
-                                                          float scale_lo,
-                                                          const double* __restrict__ damp_ptr) {
+                                                          float scale_lo, double damp_percent,
+                                                          double* __restrict__ scratch,
+                                                          float* __restrict__ damp_f32) {
     __shared__ float tr[64][65];
-    const int t = blockIdx.x;
-    const int a = blockIdx.y >> 1, b = blockIdx.y & 1;
-    int I = 0, rem = t;
-    while (rem >= T - I) {
-        rem -= T - I;
-        ++I;
+    __shared__ double wpart[8];
+    __shared__ int last;
+    const int a = (blockIdx.x >> 1) & 1, b = blockIdx.x & 1;
+    int I, J;
+    if (static_cast<int>(blockIdx.x >> 2) < T) {
+        I = J = static_cast<int>(blockIdx.x >> 2);
+    } else {
+        // strictly upper tiles, row by row
+        int rem = static_cast<int>(blockIdx.x >> 2) - T;
+        I = 0;
+        while (rem >= T - 1 - I) {
+            rem -= T - 1 - I;
+            ++I;
+        }
+        J = I + 1 + rem;
     }
-    const int J = I + rem;
     if (I == J && a > b) return;  // lower quarter of a diagonal tile: covered by its mirror
+    const int t = tile_index(I, J, T);
+    const bool diag = I == J && a == b;
     const int r0 = I * kTile + a * 64, c0 = J * kTile + b * 64;
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
     const float* tile = acc + static_cast<size_t>(t) * kTileWords;
     const int r = r0 + tx;
-    for (int q = ty; q < 16; q += 4) {
-        const int k = tile_offset(a * 64 + tx, b * 64 + 4 * q);
-        const float4 h4 = *reinterpret_cast<const float4*>(tile + k);
-        const float4 l4 = *reinterpret_cast<const float4*>(tile + kTileElems + k);
-        const float hs[4] = {h4.x, h4.y, h4.z, h4.w};
-        const float ls[4] = {l4.x, l4.y, l4.z, l4.w};
+    float4 h4[4], l4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = tile_offset(a * 64 + tx, b * 64 + 4 * (ty + 4 * i));
+        h4[i] = *reinterpret_cast<const float4*>(tile + k);
+        l4[i] = *reinterpret_cast<const float4*>(tile + kTileElems + k);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = ty + 4 * i;
+        const float hs[4] = {h4[i].x, h4[i].y, h4[i].z, h4[i].w};
+        const float ls[4] = {l4[i].x, l4[i].y, l4[i].z, l4[i].w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int c = c0 + 4 * q + m;
@@ -94,17 +92,57 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
         }
     }
     __syncthreads();
-    if (I == J && a == b) {
-        if (ty == 0 && r < d) {
-            const int k = tile_offset(a * 64 + tx, a * 64 + tx);
-            const double s = static_cast<double>(tile[k]) + static_cast<double>(tile[kTileElems + k]);
-            tr[tx][tx] = static_cast<float>(s * scale + *damp_ptr);
-        }
-        __syncthreads();
-    }
+#pragma unroll 4
     for (int rr = ty; rr < 64; rr += 4) {
         const int r2 = r0 + rr, c = c0 + tx;
-        if (r2 < d && c < d && r2 <= c) H[static_cast<size_t>(r2) * d + c] = tr[tx][rr];
+        if (c < d && r2 < c) H[static_cast<size_t>(r2) * d + c] = tr[tx][rr];
+    }
+    if (!diag) return;
+
+    // ---- diagonal quarter: its fp64 partial sum, then the arrival count
+    if (ty == 0) {
+        double s = 0.0;
+        if (r < d) {
+            const int k = tile_offset(a * 64 + tx, a * 64 + tx);
+            s = static_cast<double>(tile[k]) + static_cast<double>(tile[kTileElems + k]);
+        }
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if ((tx & 31) == 0) wpart[tx >> 5] = s;
+    }
+    __syncthreads();
+    unsigned* const ticket = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(scratch) + ticket_offset(T));
+    if (threadIdx.x == 0) {
+        scratch[1 + 2 * I + a] = wpart[0] + wpart[1];
+        __threadfence();
+        last = atomicAdd(ticket, 1u) == static_cast<unsigned>(2 * T - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    {
+        // the partial sums, in a fixed order: thread k takes k, k + 256, ...
+        double s = 0.0;
+        for (int i = threadIdx.x; i < 2 * T; i += blockDim.x) s += __ldcg(scratch + 1 + i);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if ((threadIdx.x & 31) == 0) wpart[threadIdx.x >> 5] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int w = 0; w < 8; ++w) s += wpart[w];
+        const double damp = damp_percent * ((s * scale) / static_cast<double>(d));
+        scratch[0] = damp;
+        *damp_f32 = static_cast<float>(damp);
+        *ticket = 0u;  // ready for the next launch (every quarter has arrived)
+        wpart[0] = damp;
+    }
+    __syncthreads();
+    const double damp = wpart[0];
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const int ti = i / kTile, rr = i % kTile;
+        const float* e = acc + static_cast<size_t>(tile_index(ti, ti, T)) * kTileWords + tile_offset(rr, rr);
+        const double v = static_cast<double>(e[0]) + static_cast<double>(e[kTileElems]);
+        H[static_cast<size_t>(i) * d + i] = static_cast<float>(v * scale + damp);
     }
 }
 
@@ -119,20 +157,15 @@ __global__ void __launch_bounds__(256) local_read_kernel(const double* __restric
 
 }  // namespace
 
-cudaError_t launch_diag_damp(const float* acc, int d, int T, double scale, double damp_percent,
-                             double* damp_out, float* damp_out_f32, cudaStream_t s) {
-    diag_damp_kernel<<<1, kDiagThreads, 0, s>>>(acc, d, T, scale, damp_percent, damp_out,
-                                                damp_out_f32);
-    return cudaGetLastError();
-}
+size_t materialize_scratch_bytes(int T) { return ticket_offset(T) + sizeof(unsigned); }
 
 cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
-                               const double* damp, cudaStream_t s) {
+                               double damp_percent, double* scratch, float* damp_f32, cudaStream_t s) {
     const int n_tiles = T * (T + 1) / 2;
     const float scale_hi = static_cast<float>(scale);
     const float scale_lo = static_cast<float>(scale - static_cast<double>(scale_hi));
-    materialize_kernel<<<dim3(n_tiles, 4), 256, 0, s>>>(acc, H_out, d, T, scale, scale_hi, scale_lo,
-                                                        damp);
+    materialize_kernel<<<4 * n_tiles, 256, 0, s>>>(acc, H_out, d, T, scale, scale_hi, scale_lo,
+                                                        damp_percent, scratch, damp_f32);
     return cudaGetLastError();
 }
 
