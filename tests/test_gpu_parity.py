@@ -1,4 +1,5 @@
-"""GPU parity of the CUDA path against the float64 oracle, small sizes.
+"""GPU parity of the CUDA path against the float64 oracle, small sizes (and
+the widest layers, on sampled columns).
 
 Every call goes through the C ABI (ctypes binding).  Sizes span several
 128x128 tiles, ragged token tails (n not a multiple of 128, n = 1), widths
@@ -13,7 +14,7 @@ import pytest
 import torch
 
 from helpers import TOL_BF16, TOL_F32, batches, block_rel_err, host, rel_err
-from oracle import GramOracle, LocalGramOracle
+from oracle import GramOracle, LocalGramOracle, column_sum_of_squares, gram_columns
 
 pytestmark = pytest.mark.gpu
 
@@ -375,3 +376,43 @@ def test_local_zero_and_reset():
     lh.reset()
     assert lh.n_tokens == 0 and not torch.any(lh.read())
     lh.close()
+
+
+@pytest.mark.parametrize("d,counts,dtype", [
+    (16376, [300, 77, 1], torch.bfloat16),
+    (12296, [40, 129], torch.float32),
+])
+def test_wide_ragged_width(d, counts, dtype):
+    """The widest layers: 8,256 upper tiles at d = 16,376, with a last tile
+    row 120 wide (d is a multiple of 8 but not of 128).  The oracle computes
+    a seeded sample of whole columns, the last column included, and the full
+    diagonal (which fixes the damping)."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    cols = np.sort(np.concatenate([np.random.default_rng(7).choice(d - 1, 11, replace=False), [d - 1]]))
+    h = Hessian(d)
+    S = np.zeros((d, cols.size))
+    sq = np.zeros(d)
+    N = 0
+    for X in batches(d, counts, seed=31, dtype=dtype):
+        h.add_batch(X)
+        Xh = host(X)
+        part, n = gram_columns([Xh], cols)
+        S += part
+        sq += column_sum_of_squares([Xh])[0]
+        N += n
+    H, damp = h.materialize(0.01)
+    h.sync()
+    assert h.n_tokens == N == sum(counts)
+    scale = 2.0 / N
+    mean_diag = sq.mean() * scale
+    ref = S * scale
+    ref[cols, np.arange(cols.size)] += 0.01 * mean_diag
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    got = H[:, torch.from_numpy(cols).cuda()].cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() / mean_diag <= tol
+    diag = torch.diagonal(H).cpu().numpy().astype(np.float64)
+    assert np.abs(diag - (sq * scale + 0.01 * mean_diag)).max() / mean_diag <= tol
+    assert damp == pytest.approx(0.01 * mean_diag, rel=tol)
+    rows = H[torch.from_numpy(cols).cuda(), :].cpu().numpy()
+    assert np.array_equal(rows.T, got.astype(np.float32))
+    h.close()
