@@ -27,9 +27,10 @@
 //     atomics when several slabs add to one tile).  Warpgroup 0 (warps 0-3)
 //     gives registers to the epilogue warpgroups with setmaxnreg.
 // Why the short chains: tcgen05 accumulation into tensor memory rounds
-// toward zero, so a chain of k MMA steps loses about k ulps of its running
-// sum (measured on GB300: relative bias -1.8e-6 at 1,024 tokens, -2.6e-4 at
-// 65,536).  Banks of 128 tokens keep that below 3e-7 of each entry.
+// toward zero, so each MMA step of a chain loses about half an ulp of its
+// running sum (measured on GB300: relative bias -1.8e-6 at 1,024 tokens, -2.6e-4 at
+// 65,536).  The default 384-token chunk, two 192-token chains, keeps it
+// near 3e-7 of each entry.
 // Every mbarrier wait is bounded; on timeout a status bit is set, in-flight
 // copies and MMAs are drained, tensor memory is freed and the kernel returns.
 #include "syrk_common.cuh"
