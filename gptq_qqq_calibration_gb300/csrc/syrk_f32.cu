@@ -12,16 +12,18 @@
 // How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
 //   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
 //     128-byte swizzle with 32-byte granules, the layout MN-major tf32
-//     operands need) into a 3-deep landing ring; three converter warps
-//     (warp 0 and warps 10-11) turn each landed stage into hi / lo planes of
-//     a 2-deep MMA ring, at the same byte offsets (so the swizzle carries
-//     over), and warp 0 refills a landing slot once all three have read it;
+//     operands need) into a 3-deep landing ring, and refills a landing slot
+//     once every converter has read it;
+//   * six converter warps (2-3 and 12-15) turn each landed stage into hi /
+//     lo planes of a 2-deep MMA ring, at the same byte offsets (so the
+//     swizzle carries over), each taking every sixth round of 2 KB;
 //   * warp 1 issues tcgen05.mma kind::tf32 (M=N=128, K=8): hi*hi into bank 0
 //     and the three small terms into bank 1, so they never ride on the
 //     large running sum;
-//   * warps 2-9 run the shared compensated epilogue (bank 0 + bank 1 folded
+//   * warps 4-11 run the shared compensated epilogue (bank 0 + bank 1 folded
 //     into registers by TwoSum, added to the (hi, lo) accumulator at the
-//     end of a unit).
+//     end of a unit).  Warpgroups 0 and 3 give registers to them with
+//     setmaxnreg.
 // Tensor-core accumulation rounds toward zero, so chunks are short (32
 // tokens by default: 4 hi*hi steps).  Every wait is bounded.
 #include "syrk_common.cuh"
@@ -41,11 +43,21 @@ constexpr uint32_t kBoxBytes = kKB * 128;           // 32 tokens x 32 fp32
 constexpr uint32_t kOpBytes = 4 * kBoxBytes;        // 128 features
 constexpr uint32_t kLandBytes = 2 * kOpBytes;       // A | B raw
 constexpr uint32_t kCvtBytes = 4 * kOpBytes;        // A hi | A lo | B hi | B lo
-// Converters: warp 0 (also the TMA producer) and the two warps after the
-// epilogue warps; each takes every kCvtWarps-th round of 256 words.
-constexpr int kCvtWarps = 3;
-constexpr int kFirstExtraCvt = 2 + kEpiWarps;  // warps 10 and 11
-constexpr int kThreads = (2 + kEpiWarps + kCvtWarps - 1) * 32;
+// Warpgroup 0: warp 0 (producer), warp 1 (MMA issuer), warps 2-3
+// (converters 0-1); warpgroups 1-2: the epilogue; warpgroup 3: converters
+// 2-5.  Converter ci takes rounds ci, ci + kCvtWarps, ... of kRoundWords
+// 16-byte words.  The launch gives every thread kRegsLaunch registers;
+// warpgroups 0 and 3 hand most of theirs to the epilogue's (hi, lo) state.
+constexpr int kCvtWarps = 6;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kFirstHighCvt = kFirstEpiWarp + kEpiWarps;  // warps 12-15
+constexpr int kThreads = (kFirstHighCvt + 4) * 32;
+constexpr int kRoundWords = 128;
+constexpr uint32_t kRegsLaunch = 128;  // 65536 / 512
+constexpr uint32_t kRegsLow = 64;
+constexpr uint32_t kRegsHigh = 192;
+static_assert(2 * 128 * kRegsLow + kEpiWarps * 32 * kRegsHigh <= kThreads * kRegsLaunch,
+              "register re-split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(2u /*tf32*/, 128, 128);
 constexpr int kNumBarriers = 2 * kLand + 2 * kCvt + 5;
@@ -153,22 +165,33 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             !mbar_wait(cvt_empty(c), ((converted / kCvt) & 1u) ^ 1u, limit))
             return false;
         const bool diag = C.un.I == C.un.J;
-        constexpr int kRoundsPerOp = static_cast<int>(kOpBytes / 16 / 256);  // 256 words per round
+        constexpr int kRoundsPerOp = static_cast<int>(kOpBytes / 16 / kRoundWords);
+        constexpr int kLd = kRoundWords / 32;  // 16-byte loads per lane per round
         const int n_rounds = (diag ? 1 : 2) * kRoundsPerOp;
         const uint32_t src = base + s * kLandBytes;
         const uint32_t dst = base + kCvtBase + c * kCvtBytes;
+        // the word of load k of round rr, for this lane, within its operand
+        auto word = [&](int rr, int k) { return ((rr % kRoundsPerOp) * kLd + k) * 32 + lane; };
 #pragma unroll 1
-        for (int rr = ci; rr < n_rounds; rr += kCvtWarps) {
-            const int op = rr / kRoundsPerOp, r = rr % kRoundsPerOp;
-            const uint32_t sp = src + op * kOpBytes;
-            const uint32_t hp = dst + op * 2 * kOpBytes;
-            const uint32_t lp = hp + kOpBytes;
-            uint4 x[8];
+        for (int rr = ci; rr < n_rounds; rr += 2 * kCvtWarps) {
+            // two rounds' loads in flight when this warp has a second one
+            const int rr2 = rr + kCvtWarps;
+            const bool two = rr2 < n_rounds;
+            uint4 x[2 * kLd];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = lds128(sp + ((r * 8 + k) * 32 + lane) * 16);
+            for (int k = 0; k < kLd; ++k) x[k] = lds128(src + (rr / kRoundsPerOp) * kOpBytes + word(rr, k) * 16);
+            if (two) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = ((r * 8 + k) * 32 + lane) * 16;
+                for (int k = 0; k < kLd; ++k)
+                    x[kLd + k] = lds128(src + (rr2 / kRoundsPerOp) * kOpBytes + word(rr2, k) * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 2 * kLd; ++k) {
+                if (k >= kLd && !two) break;
+                const int q = k < kLd ? rr : rr2;
+                const uint32_t hp = dst + (q / kRoundsPerOp) * 2 * kOpBytes;
+                const uint32_t lp = hp + kOpBytes;
+                const uint32_t off = word(q, k % kLd) * 16;
                 float h0, h1, h2, h3, l0, l1, l2, l3;
                 split_tf32(__uint_as_float(x[k].x), h0, l0);
                 split_tf32(__uint_as_float(x[k].y), h1, l1);
@@ -191,60 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
         return true;
     };
 
-    if (warp == 0) {
-        // ---------------------------------- TMA producer + converter 0
-        bool ok = true;
-        Cursor L, C;
-        cursor_start(p, L);
-        cursor_start(p, C);
-        uint32_t issued = 0, converted = 0;
-        auto issue = [&]() -> bool {
-            const int s = issued % kLand;
-            // a reused landing slot must have been read by every converter
-            if (issued >= static_cast<uint32_t>(kLand) &&
-                !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit))
-                return false;
-            const bool diag = L.un.I == L.un.J;
-            if (lane == 0) {
-                const CUtensorMap* m = &p.maps[L.b];
-                const int tok = (L.kb - p.kb_start[L.b]) * kKB;
-                const uint32_t dst = base + s * kLandBytes;
-                mbar_arrive_expect_tx(land_full(s), diag ? kOpBytes : kLandBytes);
-                for (int bx = 0; bx < 4; ++bx)
-                    tma_load_2d(dst + bx * kBoxBytes, m, land_full(s), L.un.I * kTile + 32 * bx, tok);
-                if (!diag)
-                    for (int bx = 0; bx < 4; ++bx)
-                        tma_load_2d(dst + kOpBytes + bx * kBoxBytes, m, land_full(s),
-                                    L.un.J * kTile + 32 * bx, tok);
-            }
-            __syncwarp();
-            ++issued;
-            cursor_next(p, L);
-            return true;
-        };
-        while (L.valid && issued < static_cast<uint32_t>(kLand)) issue();
-        while (ok && C.valid) {
-            if (!convert_stage(0, C, converted)) {
-                ok = false;
-                break;
-            }
-            ++converted;
-            cursor_next(p, C);
-            if (L.valid && !issue()) ok = false;
-        }
-        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
-        // Every issued copy must land before the CTA may exit.
-        if (lane == 0) {
-            for (uint32_t k = converted; k < issued; ++k) {
-                if (!mbar_wait(land_full(k % kLand), (k / kLand) & 1u, kDrainLimitNs)) {
-                    atomicOr(p.status, kStatusTimeoutDrain);
-                    break;
-                }
-            }
-        }
-    } else if (warp >= kFirstExtraCvt) {
-        // ---------------------------------- converters 1 and 2
-        const int ci = warp - kFirstExtraCvt + 1;
+    // Converter ci walks every (unit, k-block) of this CTA in order.
+    auto run_converter = [&](int ci) {
         Cursor C;
         cursor_start(p, C);
         uint32_t converted = 0;
@@ -258,7 +229,51 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             cursor_next(p, C);
         }
         if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
-    } else if (warp == 1) {
+    };
+
+    if (warp < kFirstEpiWarp || warp >= kFirstHighCvt) {
+      setmaxnreg_dec<kRegsLow>();
+      if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            Cursor L;
+            cursor_start(p, L);
+            uint32_t issued = 0;
+            while (L.valid) {
+                const int s = issued % kLand;
+                // a reused landing slot must have been read by every converter
+                if (issued >= static_cast<uint32_t>(kLand) &&
+                    !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit)) {
+                    ok = false;
+                    break;
+                }
+                const bool diag = L.un.I == L.un.J;
+                const CUtensorMap* m = &p.maps[L.b];
+                const int tok = (L.kb - p.kb_start[L.b]) * kKB;
+                const uint32_t dst = base + s * kLandBytes;
+                mbar_arrive_expect_tx(land_full(s), diag ? kOpBytes : kLandBytes);
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, m, land_full(s), L.un.I * kTile + 32 * bx, tok);
+                if (!diag)
+                    for (int bx = 0; bx < 4; ++bx)
+                        tma_load_2d(dst + kOpBytes + bx * kBoxBytes, m, land_full(s),
+                                    L.un.J * kTile + 32 * bx, tok);
+                ++issued;
+                cursor_next(p, L);
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
+            // Every issued copy must land before the CTA may exit: the last
+            // copy of each slot (earlier ones landed before their slot was reused).
+            const uint32_t first = issued > static_cast<uint32_t>(kLand) ? issued - kLand : 0u;
+            for (uint32_t k = first; k < issued; ++k) {
+                if (!mbar_wait(land_full(k % kLand), (k / kLand) & 1u, kDrainLimitNs)) {
+                    atomicOr(p.status, kStatusTimeoutDrain);
+                    break;
+                }
+            }
+        }
+      } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = true;
@@ -317,9 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             tc_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, kDrainLimitNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
+      } else {
+        // ------------------------------------------------ converters
+        run_converter(warp < kFirstEpiWarp ? warp - 2 : warp - kFirstHighCvt + 2);
+      }
     } else {
-        // ------------------------------------------------ epilogue (warps 2-9)
-        syrk::epilogue<kExcl, 0>(p, tmem, warp, lane, 2, accf_bar(0), acce_bar(0), limit);
+        // ------------------------------------------------ epilogue (warps 4-11)
+        setmaxnreg_inc<kRegsHigh>();
+        syrk::epilogue<kExcl, 0>(p, tmem, warp, lane, kFirstEpiWarp, accf_bar(0), acce_bar(0), limit);
     }
 
     tc_fence_before();
@@ -345,7 +365,16 @@ cudaError_t syrk_f32_prepare() {
     int blocks = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, syrk_f32_kernel<false>, kThreads, kSmemBytes);
     if (e == cudaSuccess && blocks < 1) e = cudaErrorLaunchOutOfResources;
-    return e;
+    if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the CTA's pool has the registers: the pool
+    // must be what the re-split was sized for, or the epilogue would never start.
+    for (auto fn : {syrk_f32_kernel<false>, syrk_f32_kernel<true>}) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorLaunchOutOfResources;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s) {
