@@ -29,6 +29,7 @@ METRIC = "Hessian-accum TFLOP/s & tokens/s at d=4096 (1 GB300); % of BF16/HBM ro
 # DRAM bytes (read + write) per SYRK launch of one step of the default workload, from an ncu
 # capture of the current kernel (profiles/syrk_bf16_d4096_ragged360_dram.md); set to None when
 # the kernel changes until it is captured again.
+F32_MMAS = 3  # tf32 MMAs per product in the fp32-input kernel
 SYRK_DRAM_BYTES_PER_LAUNCH = {"d4096_ragged360_loguniform": 1.752e9}
 
 
@@ -430,11 +431,12 @@ def _x_f32_input_ragged(hbm, bf16_burst):
     fl = algo_flops(wl.n_tokens, wl.d)
     t = kern["seconds"]
     tf32_peak = bf16_burst / 2.0  # dense tf32 runs at half the bf16 rate
+    # hi*hi, hi*lo and lo*hi: three tf32 MMAs of the algorithmic product each
     out["f32_input_ragged"] = {
         "workload": wl.name + " (fp32 input)", "tflops": round(fl / t / 1e12, 2), "ms": round(t * 1e3, 3),
-        "tokens_per_s": round(wl.n_tokens / t, 1), "mma_per_8_tokens": 4,
-        "roofline": {"bound": "tensor", "achieved_tf32": round(4 * fl / t / 1e12, 2), "peak": tf32_peak,
-                     "unit": "TFLOP/s", "frac": round(4 * fl / t / 1e12 / tf32_peak, 4),
+        "tokens_per_s": round(wl.n_tokens / t, 1), "mma_per_8_tokens": F32_MMAS,
+        "roofline": {"bound": "tensor", "achieved_tf32": round(F32_MMAS * fl / t / 1e12, 2), "peak": tf32_peak,
+                     "unit": "TFLOP/s", "frac": round(F32_MMAS * fl / t / 1e12 / tf32_peak, 4),
                      "peak_source": "bf16_tflops (burst) x 1/2 (nominal tf32:bf16 ratio)"}}
     h.close()
     return out["f32_input_ragged"]

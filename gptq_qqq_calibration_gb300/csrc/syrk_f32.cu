@@ -5,9 +5,11 @@
 // do?").  Here the same sums run on the tensor cores with a split that keeps
 // fp32 accuracy: every value is written x = hi + lo, hi = x rounded to
 // nearest tf32 (11 significant bits) and lo = x - hi (exact), and
-//     x_i x_j = hi_i hi_j + (hi_i lo_j + lo_i hi_j + lo_i lo_j)
-// where only the tf32 rounding of lo (relative 2^-22 of x, zero mean because
-// hi is rounded to nearest) is lost.
+//     x_i x_j ~ hi_i hi_j + (hi_i lo_j + lo_i hi_j)
+// The tf32 rounding of lo (relative 2^-22 of x, zero mean because hi is
+// rounded to nearest) is lost, and so is lo_i lo_j: below 2^-24 of x_i x_j,
+// the size of one fp32 rounding of the product, and never negative on the
+// diagonal (a bias of about -2e-8 of each diagonal entry).
 //
 // How (same skeleton as the bf16 kernel, 128x128 tiles, 32-token k-blocks):
 //   * warp 0 lane 0 stages raw fp32 boxes (32 tokens x 32 features,
@@ -18,8 +20,8 @@
 //     lo planes of a 2-deep MMA ring, at the same byte offsets (so the
 //     swizzle carries over), each taking every sixth round of 2 KB;
 //   * warp 1 issues tcgen05.mma kind::tf32 (M=N=128, K=8): hi*hi into bank 0
-//     and the three small terms into bank 1, so they never ride on the
-//     large running sum;
+//     and the two cross terms into bank 1, so they never ride on the large
+//     running sum;
 //   * warps 4-11 run the shared compensated epilogue (bank 0 + bank 1 folded
 //     into registers by TwoSum, added to the (hi, lo) accumulator at the
 //     end of a unit).  Warpgroups 0 and 3 give registers to them with
@@ -315,7 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
                             umma_tf32(d0, ahi, bhi, kIdesc, acc);
                             umma_tf32(d1, ahi, blo, kIdesc, acc);
                             umma_tf32(d1, alo, bhi, kIdesc, 1u);
-                            umma_tf32(d1, alo, blo, kIdesc, 1u);
                         }
                         tc_commit(cvt_empty(cs));
                         ++consumed;
