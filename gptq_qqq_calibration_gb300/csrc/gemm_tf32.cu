@@ -19,11 +19,13 @@
 // tile's MMAs.  Warp roles follow the fp32 SYRK kernel:
 //   * warp 0 lane 0 stages 32 x 32 fp32 boxes of P and Q (128-byte swizzle,
 //     32-byte granules: the MN-major tf32 layout) into a 3-deep landing ring;
-//     warps 0, 10 and 11 split each landed stage into hi / lo planes of a
-//     2-deep ring at the same offsets;
+//   * six converter warps (2-3 and 12-15) split each landed stage into hi /
+//     lo planes of a 2-deep ring at the same offsets, each taking every
+//     sixth 2 KB round;
 //   * warp 1 lane 0 issues tcgen05.mma kind::tf32 (M = N = 128, K = 8);
-//   * warps 2-9 add bank 0 + bank 1 and write C[r][c] += alpha * sum, a
+//   * warps 4-11 add bank 0 + bank 1 and write C[r][c] += alpha * sum, a
 //     warp's 32 lanes covering 32 consecutive columns of one row.
+//     Warpgroups 0 and 3 give registers to them with setmaxnreg.
 // Tensor-memory accumulation rounds toward zero; with K <= 512 (64 steps
 // per bank) the drift is ~1e-6 of each update.  Every wait is bounded.
 #include <cuda.h>
@@ -42,9 +44,20 @@ constexpr uint32_t kOpBytes = 4 * kBoxBytes;          // 128 columns
 constexpr uint32_t kLandBytes = 2 * kOpBytes;         // Q | P raw
 constexpr uint32_t kCvtBytes = 4 * kOpBytes;          // Q hi | Q lo | P hi | P lo
 constexpr int kEpiWarps = 8;
-constexpr int kCvtWarps = 3;
-constexpr int kFirstExtraCvt = 2 + kEpiWarps;         // warps 10 and 11
-constexpr int kThreads = (2 + kEpiWarps + kCvtWarps - 1) * 32;
+// Warpgroup 0: warp 0 (producer), warp 1 (MMA issuer), warps 2-3
+// (converters 0-1); warpgroups 1-2: the write-back; warpgroup 3:
+// converters 2-5.  Converter ci takes rounds ci, ci + kCvtWarps, ... of
+// kRoundWords 16-byte words.
+constexpr int kCvtWarps = 6;
+constexpr int kFirstEpiWarp = 4;
+constexpr int kFirstHighCvt = kFirstEpiWarp + kEpiWarps;  // warps 12-15
+constexpr int kThreads = (kFirstHighCvt + 4) * 32;
+constexpr int kRoundWords = 128;
+constexpr uint32_t kRegsLaunch = 128;  // 65536 / 512
+constexpr uint32_t kRegsLow = 64;
+constexpr uint32_t kRegsHigh = 192;
+static_assert(2 * 128 * kRegsLow + kEpiWarps * 32 * kRegsHigh <= kThreads * kRegsLaunch,
+              "register re-split exceeds the launch's registers");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = instr_desc_mn_major(2u /*tf32*/, 128, 128);
 // land_full, land_empty (kLand each); cvt_full, cvt_empty (kCvt each);
@@ -150,21 +163,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
         if (!mbar_wait(land_full(s), (converted / kLand) & 1u, limit) ||
             !mbar_wait(cvt_empty(c), ((converted / kCvt) & 1u) ^ 1u, limit))
             return false;
-        constexpr int kRoundsPerOp = static_cast<int>(kOpBytes / 16 / 256);  // 256 words per round
+        constexpr int kRoundsPerOp = static_cast<int>(kOpBytes / 16 / kRoundWords);
+        constexpr int kLd = kRoundWords / 32;  // 16-byte loads per lane per round
+        constexpr int n_rounds = 2 * kRoundsPerOp;
         const uint32_t src = base + s * kLandBytes;
         const uint32_t dst = base + kCvtBase + c * kCvtBytes;
+        // the word of load k of round rr, for this lane, within its operand
+        auto word = [&](int rr, int k) { return ((rr % kRoundsPerOp) * kLd + k) * 32 + lane; };
 #pragma unroll 1
-        for (int rr = ci; rr < 2 * kRoundsPerOp; rr += kCvtWarps) {
-            const int op = rr / kRoundsPerOp, r = rr % kRoundsPerOp;
-            const uint32_t sp = src + op * kOpBytes;
-            const uint32_t hp = dst + op * 2 * kOpBytes;
-            const uint32_t lp = hp + kOpBytes;
-            uint4 x[8];
+        for (int rr = ci; rr < n_rounds; rr += 2 * kCvtWarps) {
+            // two rounds' loads in flight when this warp has a second one
+            const int rr2 = rr + kCvtWarps;
+            const bool two = rr2 < n_rounds;
+            uint4 x[2 * kLd];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = lds128(sp + ((r * 8 + k) * 32 + lane) * 16);
+            for (int k = 0; k < kLd; ++k) x[k] = lds128(src + (rr / kRoundsPerOp) * kOpBytes + word(rr, k) * 16);
+            if (two) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = ((r * 8 + k) * 32 + lane) * 16;
+                for (int k = 0; k < kLd; ++k)
+                    x[kLd + k] = lds128(src + (rr2 / kRoundsPerOp) * kOpBytes + word(rr2, k) * 16);
+            }
+#pragma unroll
+            for (int k = 0; k < 2 * kLd; ++k) {
+                if (k >= kLd && !two) break;
+                const int q = k < kLd ? rr : rr2;
+                const uint32_t hp = dst + (q / kRoundsPerOp) * 2 * kOpBytes;
+                const uint32_t lp = hp + kOpBytes;
+                const uint32_t off = word(q, k % kLd) * 16;
                 float h0, h1, h2, h3, l0, l1, l2, l3;
                 split_tf32(__uint_as_float(x[k].x), h0, l0);
                 split_tf32(__uint_as_float(x[k].y), h1, l1);
@@ -187,57 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
         return true;
     };
 
-    if (warp == 0) {
-        // ---------------------------------- TMA producer + converter 0
-        bool ok = true;
-        Cursor L, C;
-        cur_start(p, L);
-        cur_start(p, C);
-        uint32_t issued = 0, converted = 0;
-        auto issue = [&]() -> bool {
-            const int s = issued % kLand;
-            if (issued >= static_cast<uint32_t>(kLand) &&
-                !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit))
-                return false;
-            if (lane == 0) {
-                int n0, m0;  // first C column (Q) and row (P)
-                unit_tile(p, L.u, n0, m0);
-                const int k0 = L.kb * kKB;
-                const uint32_t dst = base + s * kLandBytes;
-                mbar_arrive_expect_tx(land_full(s), kLandBytes);
-                for (int bx = 0; bx < 4; ++bx)
-                    tma_load_2d(dst + bx * kBoxBytes, &p.q_map, land_full(s), n0 + 32 * bx, k0);
-                for (int bx = 0; bx < 4; ++bx)
-                    tma_load_2d(dst + kOpBytes + bx * kBoxBytes, &p.p_map, land_full(s), m0 + 32 * bx, k0);
-            }
-            __syncwarp();
-            ++issued;
-            cur_next(p, L);
-            return true;
-        };
-        while (L.valid && issued < static_cast<uint32_t>(kLand)) issue();
-        while (ok && C.valid) {
-            if (!convert_stage(0, converted)) {
-                ok = false;
-                break;
-            }
-            ++converted;
-            cur_next(p, C);
-            if (L.valid && !issue()) ok = false;
-        }
-        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
-        // Every issued copy must land before the CTA may exit.
-        if (lane == 0) {
-            for (uint32_t k = converted; k < issued; ++k) {
-                if (!mbar_wait(land_full(k % kLand), (k / kLand) & 1u, kDrainNs)) {
-                    atomicOr(p.status, kStatusTimeoutDrain);
-                    break;
-                }
-            }
-        }
-    } else if (warp >= kFirstExtraCvt) {
-        // ---------------------------------- converters 1 and 2
-        const int ci = warp - kFirstExtraCvt + 1;
+    // Converter ci walks every (tile, k-block) of this CTA in order.
+    auto run_converter = [&](int ci) {
         Cursor C;
         cur_start(p, C);
         uint32_t converted = 0;
@@ -251,7 +227,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
             cur_next(p, C);
         }
         if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutLoad);
-    } else if (warp == 1) {
+    };
+
+    if (warp < kFirstEpiWarp || warp >= kFirstHighCvt) {
+      setmaxnreg_dec<kRegsLow>();
+      if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            Cursor L;
+            cur_start(p, L);
+            uint32_t issued = 0;
+            while (L.valid) {
+                const int s = issued % kLand;
+                // a reused landing slot must have been read by every converter
+                if (issued >= static_cast<uint32_t>(kLand) &&
+                    !mbar_wait(land_empty(s), ((issued / kLand) + 1u) & 1u, limit)) {
+                    ok = false;
+                    break;
+                }
+                int n0, m0;  // first C column (Q) and row (P)
+                unit_tile(p, L.u, n0, m0);
+                const int k0 = L.kb * kKB;
+                const uint32_t dst = base + s * kLandBytes;
+                mbar_arrive_expect_tx(land_full(s), kLandBytes);
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + bx * kBoxBytes, &p.q_map, land_full(s), n0 + 32 * bx, k0);
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(dst + kOpBytes + bx * kBoxBytes, &p.p_map, land_full(s), m0 + 32 * bx, k0);
+                ++issued;
+                cur_next(p, L);
+            }
+            if (!ok) atomicOr(p.status, kStatusTimeoutLoad);
+            // Every issued copy must land before the CTA may exit: the last
+            // copy of each slot (earlier ones landed before their slot was reused).
+            const uint32_t first = issued > static_cast<uint32_t>(kLand) ? issued - kLand : 0u;
+            for (uint32_t k = first; k < issued; ++k) {
+                if (!mbar_wait(land_full(k % kLand), (k / kLand) & 1u, kDrainNs)) {
+                    atomicOr(p.status, kStatusTimeoutDrain);
+                    break;
+                }
+            }
+        }
+      } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = true;
@@ -302,12 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tf32_kernel(const __grid_con
             tc_commit(drain_bar);
             if (!mbar_wait(drain_bar, 0, kDrainNs)) atomicOr(p.status, kStatusTimeoutDrain);
         }
+      } else {
+        // ------------------------------------------------ converters
+        run_converter(warp < kFirstEpiWarp ? warp - 2 : warp - kFirstHighCvt + 2);
+      }
     } else {
-        // ------------------------------------------------ write-back (warps 2-9)
+        // ------------------------------------------------ write-back (warps 4-11)
         // Warp w reads tensor-memory lanes 32 (w % 4) .. +31 (C columns) and
         // 64 of the tile's 128 C rows.
+        setmaxnreg_inc<kRegsHigh>();
         const int q = warp & 3;
-        const int part = (warp - 2) >> 2;
+        const int part = (warp - kFirstEpiWarp) >> 2;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         bool ok = true;
         int ab = 0;
@@ -404,7 +427,14 @@ cudaError_t gemm_tf32_prepare() {
     int blocks = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemm_tf32_kernel, kThreads, kSmemBytes);
     if (e == cudaSuccess && blocks < 1) e = cudaErrorLaunchOutOfResources;
-    return e;
+    if (e != cudaSuccess) return e;
+    // setmaxnreg.inc waits until the CTA's pool has the registers: the pool
+    // must be what the re-split was sized for, or the write-back would never start.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gemm_tf32_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorLaunchOutOfResources;
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, float* C, int ldc, int M, int N,
