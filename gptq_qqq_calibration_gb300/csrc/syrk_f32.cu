@@ -26,8 +26,8 @@
 //     into registers by TwoSum, added to the (hi, lo) accumulator at the
 //     end of a unit).  Warpgroups 0 and 3 give registers to them with
 //     setmaxnreg.
-// Tensor-core accumulation rounds toward zero, so chunks are short (32
-// tokens by default: 4 hi*hi steps).  Every wait is bounded.
+// Tensor-core accumulation rounds toward zero, so chunks are short (64
+// tokens by default: 8 hi*hi steps).  Every wait is bounded.
 #include "syrk_common.cuh"
 
 namespace hk {

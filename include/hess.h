@@ -82,8 +82,8 @@ typedef enum {
                                      default 384).  Tensor-core accumulation rounds toward
                                      zero, so longer chunks bias H low: at 384, channels whose
                                      diagonal is 80x the mean diagonal come out ~2.4e-5 of the
-                                     mean diagonal low.  fp32 batches use chunks of an eighth
-                                     of this (at least 32 tokens). */
+                                     mean diagonal low.  fp32 batches use chunks of a sixth
+                                     of this, in 32-token steps (64 by default). */
     HESS_OPT_WAIT_TIMEOUT_NS = 4, /* limit of every device-side wait, ns (default 2e9; 0 makes
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */
