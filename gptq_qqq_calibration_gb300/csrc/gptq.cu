@@ -30,6 +30,7 @@
 
 #include <cuda_bf16.h>
 
+#include "device_ptr.h"
 #include "gptq.h"
 #include "hess.h"
 #include "kernels.cuh"
@@ -782,6 +783,14 @@ hess_status gq_check_device(int dev) {
     return HESS_OK;
 }
 
+// A caller's buffer must be device memory of the handle's device (or
+// managed memory); anything else is refused before a kernel could touch it.
+hess_status gq_check_buffer(const void* p, int dev, const char* name) {
+    char why[128];
+    if (const char* w = hk::device_ptr_problem(p, dev, why)) return gq_fail(HESS_ERR_INVALID, "%s %s", name, w);
+    return HESS_OK;
+}
+
 void gq_free(gptq_ctx* g) {
     cudaFree(g->F);
     cudaFree(g->X);
@@ -960,6 +969,7 @@ GQ_EXPORT hess_status gptq_prepare(gptq_t g, const float* H, int64_t n_tokens, d
     std::lock_guard<std::mutex> lk(g->mu);
     hess_status st = gq_check_device(g->device);
     if (st != HESS_OK) return st;
+    if ((st = gq_check_buffer(H, g->device, "H")) != HESS_OK) return st;
     st = prepare_locked(g, H, damp_percent, static_cast<cudaStream_t>(stream), damp_value_out);
     if (st == HESS_OK) g->n_tokens = n_tokens;
     return st;
@@ -991,6 +1001,7 @@ GQ_EXPORT hess_status gptq_read_factor(gptq_t g, float* U_out, hess_stream_t str
     std::lock_guard<std::mutex> lk(g->mu);
     hess_status st = gq_check_device(g->device);
     if (st != HESS_OK) return st;
+    if ((st = gq_check_buffer(U_out, g->device, "U_out")) != HESS_OK) return st;
     if (!g->prepared) return gq_fail(HESS_ERR_INVALID, "no factor: gptq_prepare has not succeeded");
     GQ_TRY(cudaMemcpyAsync(U_out, g->F, static_cast<size_t>(g->d) * g->d * sizeof(float),
                            cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
@@ -1016,6 +1027,12 @@ GQ_EXPORT hess_status gptq_quantize(gptq_t g, const void* W, int32_t w_dtype, in
     std::lock_guard<std::mutex> lk(g->mu);
     hess_status st = gq_check_device(g->device);
     if (st != HESS_OK) return st;
+    if (rows > 0) {
+        if ((st = gq_check_buffer(W, g->device, "W")) != HESS_OK) return st;
+        if ((st = gq_check_buffer(Wq_out, g->device, "Wq_out")) != HESS_OK) return st;
+        if ((st = gq_check_buffer(scales_out, g->device, "scales_out")) != HESS_OK) return st;
+        if (codes_out && (st = gq_check_buffer(codes_out, g->device, "codes_out")) != HESS_OK) return st;
+    }
     if (!g->prepared) return gq_fail(HESS_ERR_INVALID, "no factor: gptq_prepare has not succeeded");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int d = static_cast<int>(g->d), n = g->n_blocks;

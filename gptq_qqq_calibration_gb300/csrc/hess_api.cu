@@ -17,6 +17,7 @@
 #include <string>
 #include <vector>
 
+#include "device_ptr.h"
 #include "hess.h"
 #include "kernels.cuh"
 
@@ -168,6 +169,14 @@ hess_status check_device(int dev) {
     CUDA_TRY(cudaGetDevice(&cur));
     if (cur != dev)
         return fail(HESS_ERR_INVALID, "handle belongs to device %d but device %d is current", dev, cur);
+    return HESS_OK;
+}
+
+// A caller's buffer must be device memory of the handle's device (or
+// managed memory); anything else is refused before a kernel could touch it.
+hess_status check_buffer(const void* p, int dev, const char* name) {
+    char why[128];
+    if (const char* w = hk::device_ptr_problem(p, dev, why)) return fail(HESS_ERR_INVALID, "%s %s", name, w);
     return HESS_OK;
 }
 
@@ -367,6 +376,7 @@ HESS_EXPORT hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(X, h->device, "X")) != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!h->pending.empty()) {
         const int64_t kb_now = ceil_div(n_tokens, hk::kKBlock);
@@ -404,6 +414,7 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(H_out, h->device, "H_out")) != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = flush_locked(h, s);
     if (st != HESS_OK) return st;
@@ -697,6 +708,7 @@ HESS_EXPORT hess_status imatrix_add(imatrix_t h, const void* X, int64_t n_tokens
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(X, h->device, "X")) != HESS_OK) return st;
     CUDA_TRY(hk::launch_colsumsq(X, dtype == HESS_F32, n_tokens, static_cast<int>(h->d), h->acc,
                                  h->sm_count, static_cast<cudaStream_t>(stream)));
     h->N += n_tokens;
@@ -709,6 +721,7 @@ HESS_EXPORT hess_status imatrix_read(imatrix_t h, float* out, hess_stream_t stre
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(out, h->device, "out")) != HESS_OK) return st;
     CUDA_TRY(hk::launch_colsumsq_read(h->acc, out, static_cast<int>(h->d),
                                       static_cast<cudaStream_t>(stream)));
     return HESS_OK;
@@ -800,6 +813,7 @@ HESS_EXPORT hess_status local_hess_add(local_hess_t h, const void* X, int64_t n_
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(X, h->device, "X")) != HESS_OK) return st;
     hk::LocalParams p;
     std::memset(&p, 0, sizeof(p));
     st = encode_2d(&p.map, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h->d, n_tokens, 64, hk::kLocalKBlock);
@@ -827,6 +841,7 @@ HESS_EXPORT hess_status local_hess_read(local_hess_t h, float* out, hess_stream_
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_buffer(out, h->device, "out")) != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->N == 0) {
         CUDA_TRY(cudaMemsetAsync(out, 0, static_cast<size_t>(h->n_blocks) * 256 * sizeof(float), s));

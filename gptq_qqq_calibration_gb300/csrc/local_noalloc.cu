@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "hess.h"
+#include "device_ptr.h"
 #include "kernels.cuh"
 
 namespace {
@@ -124,6 +125,10 @@ extern "C" __attribute__((visibility("default"))) hess_status local_hess_compute
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return noalloc_fail(HESS_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(err));
+    char why[128];
+    if (const char* w = hk::device_ptr_problem(out, dev, why)) return noalloc_fail(HESS_ERR_INVALID, "out %s", w);
+    if (n_tokens > 0)
+        if (const char* w = hk::device_ptr_problem(X, dev, why)) return noalloc_fail(HESS_ERR_INVALID, "X %s", w);
     DeviceScratch sc;
     hess_status st = scratch_for_device(dev, sc);
     if (st != HESS_OK) return st;

@@ -123,7 +123,8 @@ hess_status hess_create(int64_t d, hess_t* out);
  * hess_pending_batches() tells how many of the most recent batches are
  * still queued after a call returns.
  * Errors: INVALID (NULL handle, n_tokens < 0, NULL X with n_tokens > 0,
- * unknown dtype, X not 16-byte aligned), CUDA. */
+ * unknown dtype, X not 16-byte aligned, X not device memory of the
+ * handle's device or managed memory), CUDA. */
 hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens, int32_t dtype,
                            hess_stream_t stream);
 
@@ -146,7 +147,12 @@ hess_status hess_flush(hess_t h, hess_stream_t stream);
  *   damp_value_out : HOST pointer or NULL.  When non-NULL the call waits for
  *                    `stream` and stores fp32(damp) there.
  * The accumulator is not consumed: more batches may follow.
- * Errors: INVALID, CUDA, TIMEOUT (reported when the call waits). */
+ * Errors: INVALID (also for H_out that is not device memory of the
+ * handle's device or managed memory), CUDA, TIMEOUT (reported when the call
+ * waits).  Every other entry point that takes a device buffer (imatrix_add,
+ * imatrix_read, local_hess_add, local_hess_read,
+ * local_hess_compute_noalloc, and the gptq_* calls) refuses host memory the
+ * same way, before any launch. */
 hess_status hess_materialize(hess_t h, float* H_out, double damp_percent, hess_stream_t stream,
                              float* damp_value_out);
 

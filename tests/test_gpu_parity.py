@@ -278,6 +278,43 @@ def test_invalid_pointer_alignment_is_rejected():
     hess_destroy(h)
 
 
+def test_host_buffers_are_refused_before_any_launch():
+    """Every entry point that takes activations or an output buffer refuses
+    host memory (pageable or pinned) with INVALID and leaves the handle
+    usable: a wrong pointer must not reach a kernel."""
+    from gptq_qqq_calibration_gb300 import _lib
+    from gptq_qqq_calibration_gb300 import (hess_create, hess_destroy, imatrix_create, local_hess_create)
+    L = _lib.load()
+    d = 64
+    for pinned in (False, True):
+        Xh = torch.ones((32, d), dtype=torch.bfloat16)
+        Oh = torch.zeros((d, d), dtype=torch.float32)
+        if pinned:
+            Xh, Oh = Xh.pin_memory(), Oh.pin_memory()
+        h = hess_create(d)
+        assert L.hess_add_batch(h, Xh.data_ptr(), 32, 0, None) == _lib.HESS_ERR_INVALID
+        assert b"host memory" in L.hess_last_error()
+        assert L.hess_token_count(h) == 0
+        assert L.hess_materialize(h, Oh.data_ptr(), 0.0, None, None) == _lib.HESS_ERR_INVALID
+        X = Xh.cuda()
+        assert L.hess_add_batch(h, X.data_ptr(), 32, 0, None) == _lib.HESS_OK
+        H = torch.empty((d, d), dtype=torch.float32, device="cuda")
+        assert L.hess_materialize(h, H.data_ptr(), 0.0, None, None) == _lib.HESS_OK
+        torch.cuda.synchronize()
+        assert torch.allclose(H, torch.full_like(H, 2.0))  # (2/32) * 32 * 1 * 1
+        hess_destroy(h)
+        m = imatrix_create(d)
+        assert L.imatrix_add(m, Xh.data_ptr(), 32, 0, None) == _lib.HESS_ERR_INVALID
+        assert L.imatrix_destroy(m) == _lib.HESS_OK
+        lh = local_hess_create(d)
+        assert L.local_hess_add(lh, Xh.data_ptr(), 32, d, 16, 0, None) == _lib.HESS_ERR_INVALID
+        assert L.local_hess_destroy(lh) == _lib.HESS_OK
+        Lo = torch.zeros((d // 16, 16, 16), dtype=torch.float32)
+        assert L.local_hess_compute_noalloc(X.data_ptr(), 32, d, 16, 0, Lo.data_ptr(), None) == _lib.HESS_ERR_INVALID
+        assert L.local_hess_compute_noalloc(Xh.data_ptr(), 32, d, 16, 0, Lo.cuda().data_ptr(), None) == \
+            _lib.HESS_ERR_INVALID
+
+
 def test_chunk_option_is_whole_pipeline_stages():
     """bf16 chunks are whole 128-token pipeline stages: other lengths are
     rejected before any launch, and the handle stays usable."""
