@@ -453,3 +453,55 @@ def test_wide_ragged_width(d, counts, dtype):
     rows = H[torch.from_numpy(cols).cuda(), :].cpu().numpy()
     assert np.array_equal(rows.T, got.astype(np.float32))
     h.close()
+
+
+def test_one_handle_fed_from_several_host_threads():
+    """Calls on one handle are serialised by its mutex: four host threads
+    add 80 ragged batches at once, each on its own CUDA stream, through the
+    C ABI (ctypes releases the interpreter lock during the call); two others
+    poll the token count meanwhile.  The sum must be the oracle's whatever
+    the order, and N must count every token once."""
+    import threading
+    from gptq_qqq_calibration_gb300 import _lib, hess_create, hess_destroy
+    L = _lib.load()
+    d = 384
+    counts = np.random.default_rng(41).integers(1, 700, size=80)
+    xs = list(batches(d, counts, seed=42))
+    torch.cuda.synchronize()
+    o = GramOracle(d)
+    for X in xs:
+        o.add_batch(host(X))
+    h = hess_create(d)
+    L.hess_set_option(h, _lib.OPTIONS["flush_tokens"], 3000)  # many flushes while threads race
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    errors = []
+    stop = threading.Event()
+
+    def feed(k):
+        for X in xs[k::4]:
+            st = L.hess_add_batch(h, X.data_ptr(), X.shape[0], 0, streams[k].cuda_stream)
+            if st != _lib.HESS_OK:
+                errors.append((k, st, L.hess_last_error()))
+
+    def poll():
+        while not stop.is_set():
+            if L.hess_token_count(h) < 0:
+                errors.append(("count",))
+
+    pollers = [threading.Thread(target=poll) for _ in range(2)]
+    feeders = [threading.Thread(target=feed, args=(k,)) for k in range(4)]
+    for t in pollers + feeders:
+        t.start()
+    for t in feeders:
+        t.join()
+    stop.set()
+    for t in pollers:
+        t.join()
+    assert not errors, errors
+    assert L.hess_token_count(h) == int(counts.sum())
+    H = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    assert L.hess_materialize(h, H.data_ptr(), 0.0, None, None) == _lib.HESS_OK
+    assert L.hess_sync(h, None) == _lib.HESS_OK
+    torch.cuda.synchronize()
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    hess_destroy(h)
