@@ -418,8 +418,6 @@ cudaError_t encode_fp32(CUtensorMap* map, const float* ptr, int inner, int outer
 
 }  // namespace
 
-size_t gemm_tf32_smem_bytes() { return kSmemBytes; }
-
 cudaError_t gemm_tf32_prepare() {
     cudaError_t e = cudaFuncSetAttribute(gemm_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));

@@ -71,13 +71,11 @@ __host__ __device__ inline int tile_index(int I, int J, int T) {
     return I * T - (I * (I - 1)) / 2 + (J - I);
 }
 
-size_t syrk_bf16_smem_bytes();
 cudaError_t syrk_bf16_prepare();  // sets the dynamic shared-memory limit (per device)
 cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s);
 
 // Pair-of-SMs bf16 kernel (256 x 128 tiles): n_tiles counts pair tiles,
 // sum over I2 < ceil(T/2) of (T - 2*I2); the grid is 2 CTAs per pair.
-size_t syrk_bf16_2sm_smem_bytes();
 cudaError_t syrk_bf16_2sm_prepare(int* max_pairs);
 cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s);
 __host__ __device__ inline int pair_tile_count(int T) {
@@ -101,7 +99,6 @@ struct GemmTf32Params {
     uint32_t* status;
     unsigned long long timeout_ns;
 };
-size_t gemm_tf32_smem_bytes();
 cudaError_t gemm_tf32_prepare();
 // Encodes the tensor maps and launches.  P, Q, C 16-byte aligned; ldp, ldq,
 // ldc multiples of 4; N % 128 == 0; K % 32 == 0; M >= 1.
@@ -111,7 +108,6 @@ cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, f
                              int K, float alpha, uint32_t* status, unsigned long long timeout_ns, int grid_max,
                              cudaStream_t s, bool lower = false);
 
-size_t syrk_f32_smem_bytes();
 cudaError_t syrk_f32_prepare();
 cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
 
@@ -137,7 +133,6 @@ struct LocalParams {
     int32_t total_kb;       // ceil(n / kLocalKBlock)
     int32_t chunk_steps;    // 16-token MMA steps per register chain
 };
-size_t local_smem_bytes();
 cudaError_t local_prepare();
 cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,

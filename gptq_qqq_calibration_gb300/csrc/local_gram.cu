@@ -191,8 +191,6 @@ __global__ void __launch_bounds__(kThreads) local_gram_kernel(const __grid_const
 
 }  // namespace
 
-size_t local_smem_bytes() { return kSmemBytes; }
-
 cudaError_t local_prepare() {
     return cudaFuncSetAttribute(local_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemBytes));

@@ -230,8 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
 
 }  // namespace
 
-size_t syrk_bf16_smem_bytes() { return kSmemBytes; }
-
 cudaError_t syrk_bf16_prepare() {
     cudaError_t e = cudaFuncSetAttribute(syrk_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));

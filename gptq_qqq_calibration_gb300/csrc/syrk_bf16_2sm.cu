@@ -263,8 +263,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t syrk_bf16_2sm_smem_bytes() { return kSmemBytes; }
-
 cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
     cudaError_t e = cudaFuncSetAttribute(syrk_bf16_2sm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -353,8 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
 
 }  // namespace
 
-size_t syrk_f32_smem_bytes() { return kSmemBytes; }
-
 cudaError_t syrk_f32_prepare() {
     cudaError_t e = cudaFuncSetAttribute(syrk_f32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
