@@ -83,6 +83,42 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.gptq_destroy(None) == 0
 
 
+def test_more_entry_points_reject_bad_arguments_before_cuda(lib):
+    """Merge, clone, checkpoint, imatrix and the allocation-free local call
+    refuse NULL handles and impossible sizes on the host, before any CUDA
+    call (this container has no GPU)."""
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_INVALID, HESS_ERR_UNSUPPORTED
+    h = ctypes.c_void_p()
+    n = ctypes.c_int64()
+    assert lib.hess_merge(None, None, None) == HESS_ERR_INVALID
+    assert lib.hess_clone(None, ctypes.byref(h), None) == HESS_ERR_INVALID
+    assert lib.hess_clone(None, None, None) == HESS_ERR_INVALID
+    assert lib.hess_state_bytes(None) == 0
+    assert lib.hess_export_state(None, None, 0, None, ctypes.byref(n)) == HESS_ERR_INVALID
+    assert lib.hess_import_state(None, None, 0, 0, None) == HESS_ERR_INVALID
+    assert lib.hess_pending_batches(None) == -1
+    assert lib.hess_dim(None) == -1
+    assert lib.hess_sync(None, None) == HESS_ERR_INVALID
+    assert lib.hess_reset(None, None) == HESS_ERR_INVALID
+    assert lib.imatrix_create(0, ctypes.byref(h)) == HESS_ERR_INVALID
+    assert lib.imatrix_add(None, None, 4, 0, None) == HESS_ERR_INVALID
+    assert lib.imatrix_read(None, None, None) == HESS_ERR_INVALID
+    assert lib.imatrix_token_count(None) == -1
+    assert lib.imatrix_destroy(None) == 0
+    assert lib.local_hess_read(None, None, None) == HESS_ERR_INVALID
+    assert lib.local_hess_token_count(None) == -1
+    out = ctypes.c_void_p(16)  # never dereferenced: each call fails before any CUDA call
+    assert lib.local_hess_compute_noalloc(None, -1, 64, 16, 0, out, None) == HESS_ERR_INVALID
+    assert lib.local_hess_compute_noalloc(None, 4, 0, 16, 0, out, None) == HESS_ERR_INVALID
+    assert lib.local_hess_compute_noalloc(None, 4, 64, 16, 0, None, None) == HESS_ERR_INVALID
+    assert lib.local_hess_compute_noalloc(None, 4, 64, 8, 0, out, None) == HESS_ERR_UNSUPPORTED
+    assert lib.local_hess_compute_noalloc(None, 4, 72, 16, 0, out, None) == HESS_ERR_UNSUPPORTED
+    assert lib.local_hess_compute_noalloc(None, 4, 64, 16, 1, out, None) == HESS_ERR_UNSUPPORTED
+    assert lib.local_hess_compute_noalloc(None, 4, 64, 16, 9, out, None) == HESS_ERR_INVALID
+    assert lib.local_hess_compute_noalloc(None, 4, 64, 16, 0, out, None) == HESS_ERR_INVALID  # X NULL
+    assert b"X is NULL" in lib.hess_last_error()
+
+
 def test_status_codes_match_header():
     from gptq_qqq_calibration_gb300 import _lib
     text = open(HEADER).read()
