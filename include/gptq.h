@@ -44,6 +44,10 @@ extern "C" {
 
 typedef struct gptq_ctx* gptq_t; /* workspace of one input width d */
 
+/* Every device pointer below must be device memory of the handle's device
+ * (or managed memory): host memory, pageable or pinned, and another
+ * device's memory are refused with HESS_ERR_INVALID before any launch. */
+
 /* Allocate the workspace for inputs of width d (a multiple of 128, at most
  * 32768) and weights of up to max_rows output rows: two d x d fp32 matrices
  * plus max_rows x (d + 129) fp32.  d % 128 != 0 gives HESS_ERR_UNSUPPORTED. */
