@@ -12,7 +12,6 @@ alive until the library has consumed it.
 from __future__ import annotations
 
 import ctypes
-import threading
 from typing import Optional
 
 import torch
@@ -198,30 +197,16 @@ def local_hess_destroy(h: int) -> None:
 # ------------------------------------------------------------------ objects
 
 
-def _locked(fn):
-    """Run a method under the object's lock (the borrowed-batch list)."""
-    def wrapper(self, *args, **kwargs):
-        with self._lock:
-            return fn(self, *args, **kwargs)
-    wrapper.__name__, wrapper.__doc__ = fn.__name__, fn.__doc__
-    return wrapper
-
-
 class Hessian:
-    """Accumulator of ``H = (2/N) sum x x^T`` for one layer input of width d.
-
-    Several threads may share one object: the C handle serialises its
-    calls, and a lock keeps the list of borrowed batches in step with it."""
+    """Accumulator of ``H = (2/N) sum x x^T`` for one layer input of width d."""
 
     def __init__(self, d: int, **options):
         self.d = int(d)
         self.handle = hess_create(self.d)
         self._queued = []  # batches the library still borrows, oldest first
-        self._lock = threading.Lock()
         for k, v in options.items():
             hess_set_option(self.handle, k, v)
 
-    @_locked
     def add_batch(self, X: torch.Tensor, stream=None) -> None:
         hess_add_batch(self.handle, X, self.d, stream)
         if X.numel():
@@ -236,12 +221,10 @@ class Hessian:
                 t.record_stream(cur)
             self._queued = self._queued[len(self._queued) - keep:] if keep else []
 
-    @_locked
     def flush(self, stream=None) -> None:
         hess_flush(self.handle, stream)
         self._release()
 
-    @_locked
     def materialize(self, damp_percent: float = 0.0, out: Optional[torch.Tensor] = None,
                     stream=None, want_damp: bool = True):
         if out is None:
@@ -257,7 +240,6 @@ class Hessian:
     def sync(self, stream=None) -> None:
         hess_sync(self.handle, stream)
 
-    @_locked
     def reset(self, stream=None) -> None:
         hess_reset(self.handle, stream)
         self._queued = []
@@ -267,24 +249,19 @@ class Hessian:
 
     def merge(self, other: "Hessian", stream=None) -> None:
         """Add another accumulator's sums and token count into this one."""
-        first, second = (self, other) if id(self) < id(other) else (other, self)
-        with first._lock, second._lock:  # one order for every pair: no deadlock
-            hess_merge(self.handle, other.handle, stream)
-            self._release()
-            other._release()
+        hess_merge(self.handle, other.handle, stream)
+        self._release()
+        other._release()
 
-    @_locked
     def clone(self, stream=None) -> "Hessian":
         """An independent copy of the sums, token count and options."""
         h = Hessian.__new__(Hessian)
         h.d = self.d
         h.handle = hess_clone(self.handle, stream)
         h._queued = []
-        h._lock = threading.Lock()
         self._release()
         return h
 
-    @_locked
     def export_state(self, device: str = "cpu", stream=None) -> tuple:
         """A checkpoint: (state, N), the state a uint8 tensor on `device` (host
         memory is pinned).  The copy has completed when this returns."""
@@ -296,7 +273,6 @@ class Hessian:
         self._release()
         return buf, n
 
-    @_locked
     def import_state(self, state: torch.Tensor, n_tokens: int, stream=None) -> None:
         """Resume from a checkpoint of export_state (queued batches are dropped)."""
         state = state.contiguous()
@@ -305,14 +281,10 @@ class Hessian:
         hess_sync(self.handle, stream)
 
     def close(self) -> None:
-        lock = getattr(self, "_lock", None)
-        if lock is None:
-            return
-        with lock:
-            if self.handle:
-                hess_destroy(self.handle)
-                self.handle = None
-                self._queued = []
+        if self.handle:
+            hess_destroy(self.handle)
+            self.handle = None
+            self._queued = []
 
     def __del__(self):
         try:
