@@ -91,7 +91,66 @@ def pin_damp_and_dead(quantize):
     assert res["dead"][3] and res["dead"][200] and res["dead"].sum() == 2
 
 
-ALL = [pin_loss_identity, pin_identity_hessian_is_rtn, pin_factor, pin_damp_and_dead]
+def _coupled_problem():
+    """A factor with one off-diagonal entry, U = I + a e_0 e_128^T (a = -4), so
+    that only column 0's error reaches a later column (column 128, the first
+    of the second 128-column group/block), and H_damped = U^-1 U^-T with no
+    damping.  One row with four nonzero weights."""
+    d, a = 256, -4.0
+    Uinv = np.eye(d)
+    Uinv[0, 128] = -a
+    H = Uinv @ Uinv.T  # H[0,0] = 17, H[0,128] = H[128,0] = 4, else identity
+    W = np.zeros((1, d))
+    w0, w1, w128, w129 = 0.27, 0.5, 0.6, 0.23
+    W[0, [0, 1, 128, 129]] = w0, w1, w128, w129
+    return H, W, a, (w0, w1, w128, w129)
+
+
+def pin_scale_timing_on_a_coupled_example(quantize):
+    """The scale readings of "Whole-row and grouped weight quantization"
+    (GPTQModel wiki "QQQ") on a case worked by hand.  Column 0's error
+    err0 = w0 - q0 (U_00 = 1) changes column 128 to w128 - a err0 before the
+    second block starts, and that raises the row's and the second group's
+    largest magnitude.
+      * grouped: the second group's scale comes from the updated column
+        (2 max(|w128 - a err0|, |w129|) / 15), not from the original W;
+      * whole-row: the one scale max|w| / 7 is taken before any column is
+        quantized and kept for every block (it is not re-taken from the
+        updated row)."""
+    H, W, a, (w0, w1, w128, w129) = _coupled_problem()
+
+    def rnd(x):  # round half to even, as the pages' torch.round
+        return float(np.rint(x))
+
+    # grouped, group 128: centered 4-bit codes c = clamp(round(w/s) + 8, 0, 15) - 8
+    def code_g(w, s):
+        return min(15.0, max(0.0, rnd(w / s) + 8.0)) - 8.0
+    s0 = 2.0 * max(abs(w0), abs(w1)) / 15.0
+    q0 = s0 * code_g(w0, s0)
+    w128u = w128 - a * (w0 - q0)
+    s1 = 2.0 * max(abs(w128u), abs(w129)) / 15.0
+    res = quantize(H, W, 0.0, 128)
+    assert res["scales"][0, 0] == pytest.approx(s0, rel=1e-12)
+    assert res["scales"][0, 1] == pytest.approx(s1, rel=1e-12)
+    want = {0: q0, 1: s0 * code_g(w1, s0), 128: s1 * code_g(w128u, s1), 129: s1 * code_g(w129, s1)}
+    for j, v in want.items():
+        assert res["Wq"][0, j] == pytest.approx(v, abs=1e-12), j
+
+    # whole row: signed 4-bit codes c = clamp(round(w/s), -8, 7), one scale
+    def code_r(w, s):
+        return min(7.0, max(-8.0, rnd(w / s)))
+    s = max(abs(w0), abs(w1), abs(w128), abs(w129)) / 7.0
+    q0 = s * code_r(w0, s)
+    w128u = w128 - a * (w0 - q0)
+    res = quantize(H, W, 0.0, -1)
+    assert res["scales"][0, 0] == pytest.approx(s, rel=1e-12)
+    want = {0: q0, 1: s * code_r(w1, s), 128: s * code_r(w128u, s), 129: s * code_r(w129, s)}
+    for j, v in want.items():
+        assert res["Wq"][0, j] == pytest.approx(v, abs=1e-12), j
+
+
+ALL = [pin_loss_identity, pin_identity_hessian_is_rtn, pin_factor, pin_damp_and_dead,
+       pin_scale_timing_on_a_coupled_example]
 
 
 @pytest.mark.parametrize("pin", ALL, ids=lambda f: f.__name__)
@@ -129,6 +188,7 @@ def _mutant(kind):
             U = np.linalg.cholesky(np.linalg.inv(H))
         grouped = group == 128
         rows = W.shape[0]
+        W_orig = W.copy()
         scales = np.zeros((rows, d // 128 if grouped else 1))
         if not grouped:
             scales[:, 0] = go._scale(np.max(np.abs(W), axis=1), 7.0)
@@ -138,7 +198,10 @@ def _mutant(kind):
             b1 = b0 + 128
             Err = np.zeros((rows, 128))
             if grouped:
-                scales[:, b0 // 128] = go._scale(np.max(np.abs(W[:, b0:b1]), axis=1), 7.5)
+                src = W_orig if kind == "group_scale_from_original" else W
+                scales[:, b0 // 128] = go._scale(np.max(np.abs(src[:, b0:b1]), axis=1), 7.5)
+            elif kind == "row_scale_per_block":
+                scales[:, 0] = go._scale(np.max(np.abs(W), axis=1), 7.0)
             s = scales[:, b0 // 128 if grouped else 0]
             for i in range(b0, b1):
                 w = W[:, i]
@@ -156,7 +219,8 @@ def _mutant(kind):
     return q
 
 
-@pytest.mark.parametrize("kind", ["no_divide", "lower_factor", "sign", "no_trailing", "damp_before_dead"])
+@pytest.mark.parametrize("kind", ["no_divide", "lower_factor", "sign", "no_trailing", "damp_before_dead",
+                                  "group_scale_from_original", "row_scale_per_block"])
 def test_pins_catch_planted_mistakes(kind):
     failed = 0
     for pin in ALL:
