@@ -123,6 +123,13 @@ struct hess_ctx {
     double* damp64 = nullptr;  // the damping value, then materialize's scratch
     float* damp32 = nullptr;
     cudaEvent_t ev = nullptr;
+    // Pinned host copy of the status word, refreshed by an asynchronous copy
+    // that every hess_materialize enqueues; the next call on the handle reads
+    // it once ev_status has completed, without waiting.
+    uint32_t* status_host = nullptr;
+    cudaEvent_t ev_status = nullptr;
+    bool status_copy_pending = false;
+    bool timed_out = false;  // a recorded device-side timeout was seen (until reset)
     // The accumulator's last user: work on another stream waits for it
     // (flushes may read-modify-write tiles without atomics).
     cudaEvent_t ev_acc = nullptr;
@@ -299,6 +306,18 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     return HESS_OK;
 }
 
+// A device-side timeout recorded earlier and already visible on the host
+// (from the status copy of an earlier hess_materialize) fails the call.
+hess_status check_reported(hess_ctx* h) {
+    if (h->status_copy_pending && cudaEventQuery(h->ev_status) == cudaSuccess) {
+        h->status_copy_pending = false;
+        if (*reinterpret_cast<volatile uint32_t*>(h->status_host) != 0) h->timed_out = true;
+    }
+    if (h->timed_out)
+        return fail(HESS_ERR_TIMEOUT, "a device-side wait of an earlier call ran out; hess_reset clears it");
+    return HESS_OK;
+}
+
 hess_status read_status(uint32_t* dev_status, cudaStream_t stream) {
     uint32_t st = 0;
     CUDA_TRY(cudaMemcpyAsync(&st, dev_status, sizeof(st), cudaMemcpyDeviceToHost, stream));
@@ -346,6 +365,9 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_acc, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_status, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaHostAlloc(&h->status_host, 64, cudaHostAllocDefault);
+    if (e == cudaSuccess) std::memset(h->status_host, 0, 64);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
@@ -353,8 +375,10 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
         cudaFree(h->status);
         cudaFree(h->damp64);
         cudaFree(h->damp32);
+        if (h->status_host) cudaFreeHost(h->status_host);
         if (h->ev) cudaEventDestroy(h->ev);
         if (h->ev_acc) cudaEventDestroy(h->ev_acc);
+        if (h->ev_status) cudaEventDestroy(h->ev_status);
         delete h->params;
         delete h;
         return fail(s, "hess_create: %s", cudaGetErrorString(e));
@@ -376,6 +400,7 @@ HESS_EXPORT hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_reported(h)) != HESS_OK) return st;
     if ((st = check_buffer(X, h->device, "X")) != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!h->pending.empty()) {
@@ -401,6 +426,7 @@ HESS_EXPORT hess_status hess_flush(hess_t h, hess_stream_t stream) {
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_reported(h)) != HESS_OK) return st;
     return flush_locked(h, static_cast<cudaStream_t>(stream));
 }
 
@@ -414,30 +440,36 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
+    if ((st = check_reported(h)) != HESS_OK) return st;
     if ((st = check_buffer(H_out, h->device, "H_out")) != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = flush_locked(h, s);
     if (st != HESS_OK) return st;
     if (h->N == 0) {
         CUDA_TRY(cudaMemsetAsync(H_out, 0, static_cast<size_t>(h->d) * h->d * sizeof(float), s));
-        if (damp_value_out) {
-            *damp_value_out = 0.0f;
-            return read_status(h->status, s);
-        }
-        return HESS_OK;
+    } else {
+        const double scale = 2.0 / static_cast<double>(h->N);
+        if ((st = order_acc(h, s)) != HESS_OK) return st;
+        CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, damp_percent,
+                                        h->damp64, h->damp32, s));
+        if ((st = mark_acc(h, s)) != HESS_OK) return st;
     }
-    const double scale = 2.0 / static_cast<double>(h->N);
-    if ((st = order_acc(h, s)) != HESS_OK) return st;
-    CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, damp_percent,
-                                    h->damp64, h->damp32, s));
-    if ((st = mark_acc(h, s)) != HESS_OK) return st;
     if (damp_value_out) {
         float v = 0.0f;
-        CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
+        if (h->N != 0) CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
         st = read_status(h->status, s);
-        if (st != HESS_OK) return st;
+        if (st != HESS_OK) {
+            h->timed_out = true;
+            return st;
+        }
         *damp_value_out = v;
+        return HESS_OK;
     }
+    // No wait here: the status word travels to the pinned host copy behind
+    // this call's work, and a later call reports a timeout it shows.
+    CUDA_TRY(cudaMemcpyAsync(h->status_host, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaEventRecord(h->ev_status, s));
+    h->status_copy_pending = true;
     return HESS_OK;
 }
 
@@ -460,7 +492,9 @@ HESS_EXPORT hess_status hess_sync(hess_t h, hess_stream_t stream) {
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
-    return read_status(h->status, static_cast<cudaStream_t>(stream));
+    st = read_status(h->status, static_cast<cudaStream_t>(stream));
+    if (st == HESS_ERR_TIMEOUT) h->timed_out = true;
+    return st;
 }
 
 HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
@@ -473,6 +507,8 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->pending_tokens = 0;
     h->pending_dtype = -1;
     h->N = 0;
+    h->timed_out = false;
+    h->status_copy_pending = false;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemsetAsync(h->acc, 0,
                              static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float), s));
@@ -532,8 +568,10 @@ HESS_EXPORT hess_status hess_destroy(hess_t h) {
         cudaFree(h->status);
         cudaFree(h->damp64);
         cudaFree(h->damp32);
+        cudaFreeHost(h->status_host);
         cudaEventDestroy(h->ev);
         cudaEventDestroy(h->ev_acc);
+        cudaEventDestroy(h->ev_status);
         cudaSetDevice(cur);
     }
     delete h->params;
@@ -571,20 +609,22 @@ HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream
     if (!out) return fail(HESS_ERR_INVALID, "out is NULL");
     *out = nullptr;
     if (!src) return fail(HESS_ERR_INVALID, "handle is NULL");
-    hess_t h = nullptr;
     {
         std::lock_guard<std::mutex> lk(src->mu);
         hess_status st = check_device(src->device);
         if (st != HESS_OK) return st;
-        st = flush_locked(src, static_cast<cudaStream_t>(stream));
-        if (st != HESS_OK) return st;
     }
+    // The new handle is created before src is locked (create synchronises
+    // the device); the flush, the copy and the token count are then taken
+    // under one hold of src's mutex, so a batch another thread adds to src
+    // meanwhile is either in both the copied sums and N or in neither.
+    hess_t h = nullptr;
     hess_status st = hess_create(src->d, &h);
     if (st != HESS_OK) return st;
     std::lock_guard<std::mutex> lk(src->mu);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t bytes = static_cast<size_t>(src->n_tiles) * hk::kTileWords * sizeof(float);
-    if ((st = order_acc(src, s)) != HESS_OK) {
+    if ((st = flush_locked(src, s)) != HESS_OK || (st = order_acc(src, s)) != HESS_OK) {
         hess_destroy(h);
         return st;
     }
@@ -652,6 +692,8 @@ HESS_EXPORT hess_status hess_import_state(hess_t h, const void* src, int64_t byt
     h->pending.clear();
     h->pending_tokens = 0;
     h->pending_dtype = -1;
+    h->timed_out = false;
+    h->status_copy_pending = false;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemcpyAsync(h->acc, src, static_cast<size_t>(need), cudaMemcpyDefault, s));
     CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));

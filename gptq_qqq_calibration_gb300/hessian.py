@@ -12,6 +12,7 @@ alive until the library has consumed it.
 from __future__ import annotations
 
 import ctypes
+import threading
 from typing import Optional
 
 import torch
@@ -198,39 +199,53 @@ def local_hess_destroy(h: int) -> None:
 
 
 class Hessian:
-    """Accumulator of ``H = (2/N) sum x x^T`` for one layer input of width d."""
+    """Accumulator of ``H = (2/N) sum x x^T`` for one layer input of width d.
+
+    One object may be used from several host threads: a re-entrant lock
+    makes each library call and the bookkeeping of the batches it borrows
+    one step, so a batch that another thread has just queued is never
+    released early."""
 
     def __init__(self, d: int, **options):
         self.d = int(d)
+        self._lock = threading.RLock()
         self.handle = hess_create(self.d)
         self._queued = []  # batches the library still borrows, oldest first
         for k, v in options.items():
             hess_set_option(self.handle, k, v)
 
     def add_batch(self, X: torch.Tensor, stream=None) -> None:
-        hess_add_batch(self.handle, X, self.d, stream)
-        if X.numel():
-            self._queued.append(X)
-        self._release()
+        with self._lock:
+            hess_add_batch(self.handle, X, self.d, stream)
+            if X.numel():
+                self._queued.append(X)
+            self._release(stream)
 
-    def _release(self) -> None:
+    def _release(self, stream=None) -> None:
+        """Drop the references to batches the library has flushed.  The flush
+        was enqueued on the stream of the call that triggered it (`stream`,
+        else the current stream), so each tensor is marked as in use there:
+        the caching allocator then reuses its memory only after that flush
+        has read it.  Called with the lock held."""
         keep = hess_pending_batches(self.handle)
         if keep < len(self._queued):
-            cur = torch.cuda.current_stream()
+            s = stream if stream is not None else torch.cuda.current_stream()
             for t in self._queued[: len(self._queued) - keep]:
-                t.record_stream(cur)
+                t.record_stream(s)
             self._queued = self._queued[len(self._queued) - keep:] if keep else []
 
     def flush(self, stream=None) -> None:
-        hess_flush(self.handle, stream)
-        self._release()
+        with self._lock:
+            hess_flush(self.handle, stream)
+            self._release(stream)
 
     def materialize(self, damp_percent: float = 0.0, out: Optional[torch.Tensor] = None,
                     stream=None, want_damp: bool = True):
         if out is None:
             out = torch.empty((self.d, self.d), dtype=torch.float32, device="cuda")
-        damp = hess_materialize(self.handle, out, damp_percent, stream, want_damp)
-        self._release()
+        with self._lock:
+            damp = hess_materialize(self.handle, out, damp_percent, stream, want_damp)
+            self._release(stream)
         return out, damp
 
     @property
@@ -241,25 +256,30 @@ class Hessian:
         hess_sync(self.handle, stream)
 
     def reset(self, stream=None) -> None:
-        hess_reset(self.handle, stream)
-        self._queued = []
+        with self._lock:
+            hess_reset(self.handle, stream)
+            self._queued = []
 
     def set_option(self, name: str, value: int) -> None:
         hess_set_option(self.handle, name, value)
 
     def merge(self, other: "Hessian", stream=None) -> None:
         """Add another accumulator's sums and token count into this one."""
-        hess_merge(self.handle, other.handle, stream)
-        self._release()
-        other._release()
+        first, second = sorted((self, other), key=id)  # one lock order for every pair
+        with first._lock, second._lock:
+            hess_merge(self.handle, other.handle, stream)
+            self._release(stream)
+            other._release(stream)
 
     def clone(self, stream=None) -> "Hessian":
         """An independent copy of the sums, token count and options."""
         h = Hessian.__new__(Hessian)
         h.d = self.d
-        h.handle = hess_clone(self.handle, stream)
+        h._lock = threading.RLock()
         h._queued = []
-        self._release()
+        with self._lock:
+            h.handle = hess_clone(self.handle, stream)
+            self._release(stream)
         return h
 
     def export_state(self, device: str = "cpu", stream=None) -> tuple:
@@ -268,23 +288,26 @@ class Hessian:
         buf = torch.empty(hess_state_bytes(self.handle), dtype=torch.uint8, device=device)
         if buf.device.type == "cpu":
             buf = buf.pin_memory()
-        n = hess_export_state(self.handle, buf, stream)
-        hess_sync(self.handle, stream)
-        self._release()
+        with self._lock:
+            n = hess_export_state(self.handle, buf, stream)
+            hess_sync(self.handle, stream)
+            self._release(stream)
         return buf, n
 
     def import_state(self, state: torch.Tensor, n_tokens: int, stream=None) -> None:
         """Resume from a checkpoint of export_state (queued batches are dropped)."""
         state = state.contiguous()
-        hess_import_state(self.handle, state, n_tokens, stream)
-        self._queued = []
-        hess_sync(self.handle, stream)
+        with self._lock:
+            hess_import_state(self.handle, state, n_tokens, stream)
+            self._queued = []
+            hess_sync(self.handle, stream)
 
     def close(self) -> None:
-        if self.handle:
-            hess_destroy(self.handle)
-            self.handle = None
-            self._queued = []
+        with self._lock:
+            if self.handle:
+                hess_destroy(self.handle)
+                self.handle = None
+                self._queued = []
 
     def __del__(self):
         try:

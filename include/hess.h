@@ -147,9 +147,16 @@ hess_status hess_flush(hess_t h, hess_stream_t stream);
  *   damp_value_out : HOST pointer or NULL.  When non-NULL the call waits for
  *                    `stream` and stores fp32(damp) there.
  * The accumulator is not consumed: more batches may follow.
+ * Timeouts: a device-side wait that ran out in this handle's kernels is
+ * reported (HESS_ERR_TIMEOUT) by this call when damp_value_out is non-NULL
+ * (it waits).  With NULL the call does not wait: it enqueues a copy of the
+ * handle's status word to pinned host memory, and the first later
+ * hess_add_batch, hess_flush or hess_materialize that finds that copy
+ * complete reports the timeout, before doing anything else; so does every
+ * call after it, until hess_reset or hess_import_state.  hess_sync reports
+ * it at once.
  * Errors: INVALID (also for H_out that is not device memory of the
- * handle's device or managed memory), CUDA, TIMEOUT (reported when the call
- * waits).  Every other entry point that takes a device buffer (imatrix_add,
+ * handle's device or managed memory), CUDA, TIMEOUT (above).  Every other entry point that takes a device buffer (imatrix_add,
  * imatrix_read, local_hess_add, local_hess_read,
  * local_hess_compute_noalloc, and the gptq_* calls) refuses host memory the
  * same way, before any launch. */
@@ -164,7 +171,9 @@ int64_t hess_pending_batches(hess_t h);
 int64_t hess_dim(hess_t h);
 
 /* Wait for `stream`, then report a device-side timeout recorded by any
- * kernel of this handle since the last reset (HESS_ERR_TIMEOUT), else OK. */
+ * kernel of this handle since the last reset (HESS_ERR_TIMEOUT), else OK.
+ * After a timeout, hess_add_batch, hess_flush and hess_materialize fail
+ * with HESS_ERR_TIMEOUT until hess_reset. */
 hess_status hess_sync(hess_t h, hess_stream_t stream);
 
 /* Drop queued batches, zero the accumulator (on `stream`) and set N = 0. */

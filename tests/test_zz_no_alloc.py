@@ -4,10 +4,11 @@ local_hess_compute_noalloc serves callers that may not allocate device
 memory while they run (memory reserved up front by a pooling allocator, or
 a runtime that forbids the synchronisation cudaMalloc/cudaFree can cause).
 It keeps its fp64 scratch in a fixed array inside the library, so this test
-checks two things: two calls in a row each give the same block Hessians as
-the handle-based entry points (local_hess_create / add / read, which
-allocate), within the tolerance of the other local tests; and a call
-leaves the device's free memory unchanged.
+checks three things: two calls in a row each give the same block Hessians
+as the handle-based entry points (local_hess_create / add / read, which
+allocate) and as the float64 oracle, within the tolerance of the other
+local tests, also at the largest width the scratch holds (d = 16,384); a
+call leaves the device's free memory unchanged; wider inputs are refused.
 
 This file is collected last so that a run stopping at the first failure
 has run every other test before it.
@@ -54,6 +55,14 @@ def _noalloc_result(lib, X, d, out):
     return out.cpu().numpy()
 
 
+def _oracle(X, d):
+    from oracle import LocalGramOracle
+    from helpers import host
+    o = LocalGramOracle(d)
+    o.add_batch(host(X))
+    return o.read()
+
+
 def test_noalloc_matches_handle_path_on_two_calls_in_a_row(lib):
     from gptq_qqq_calibration_gb300.synthetic import make_batch
     d = 1024
@@ -69,6 +78,26 @@ def test_noalloc_matches_handle_path_on_two_calls_in_a_row(lib):
     # the second call must not carry sums over from the first
     assert block_rel_err(got0, refs[0].astype(np.float64)) <= TOL_BF16
     assert block_rel_err(got1, refs[1].astype(np.float64)) <= TOL_BF16
+    # and each call equals the float64 oracle of its own batch
+    assert block_rel_err(got0, _oracle(xs[0], d)) <= TOL_BF16
+    assert block_rel_err(got1, _oracle(xs[1], d)) <= TOL_BF16
+
+
+def test_noalloc_at_its_width_limit(lib):
+    """d = 16,384 fills the whole scratch array (1,024 blocks): two calls in
+    a row, each graded against the float64 oracle of its own batch."""
+    from gptq_qqq_calibration_gb300.synthetic import make_batch
+    d = 16384
+    xs = [make_batch(n, d, 950 + k, profile="student_t", profile_seed=10, device="cuda")
+          for k, n in enumerate((300, 129))]
+    out = torch.empty((d // 16, 16, 16), dtype=torch.float32, device="cuda")
+    got0 = _noalloc_result(lib, xs[0], d, out)
+    free0, _ = torch.cuda.mem_get_info()
+    got1 = _noalloc_result(lib, xs[1], d, out)
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, "the no-alloc entry point changed free device memory"
+    assert block_rel_err(got0, _oracle(xs[0], d)) <= TOL_BF16
+    assert block_rel_err(got1, _oracle(xs[1], d)) <= TOL_BF16
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
