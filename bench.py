@@ -11,12 +11,20 @@ oracle instead, on a bounded sample of the same workload.
 
 from __future__ import annotations
 
-import argparse
-import json
 import os
+
+# The CPU baseline's BLAS thread count is set explicitly, before numpy loads
+# its BLAS: every host core unless the caller chose otherwise.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(os.cpu_count() or 1))
+
+import argparse
+import hashlib
+import json
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -26,11 +34,36 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Hessian-accum TFLOP/s & tokens/s at d=4096 (1 GB300); % of BF16/HBM roofline"
 
-# DRAM bytes (read + write) per SYRK launch of one step of the default workload, from an ncu
-# capture of the current kernel (profiles/syrk_bf16_d4096_ragged360_dram.md); set to None when
-# the kernel changes until it is captured again.
 F32_MMAS = 3  # tf32 MMAs per product in the fp32-input kernel
-SYRK_DRAM_BYTES_PER_LAUNCH = {"d4096_ragged360_loguniform": 1.752e9}
+
+# DRAM bytes (read + write) per SYRK launch of one step of a workload, from an
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
+# of the kernel sources it was taken on.  When the sources differ the figure
+# no longer describes the kernel and the line reports traffic as null.
+SYRK_SOURCES = ["syrk_bf16.cu", "syrk_common.cuh", "ptx.cuh", "kernels.cuh"]
+SYRK_DRAM_BYTES_PER_LAUNCH = {
+    # workload: (bytes per launch, sources hash)
+    "d4096_ragged360_loguniform": (1.752e9, None),
+}
+
+
+def syrk_source_hash():
+    h = hashlib.sha256()
+    for f in SYRK_SOURCES:
+        with open(os.path.join(ROOT, "gptq_qqq_calibration_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def syrk_traffic(workload):
+    rec = SYRK_DRAM_BYTES_PER_LAUNCH.get(workload)
+    if rec is None:
+        return None, "no capture for this workload"
+    nbytes, src = rec
+    cur = syrk_source_hash()
+    if src != cur:
+        return None, f"stale: captured on kernel sources {src}, current {cur}"
+    return nbytes, f"ncu dram bytes per launch, kernel sources {cur}"
 
 
 def peaks():
@@ -151,35 +184,63 @@ def run_ours(args):
     h = Hessian(d)
     out = torch.empty((d, d), dtype=torch.float32, device="cuda")
 
-    def step():
+    # The queue flushes at the same calls in every step (the same batches in
+    # the same order): find them once, then time each flushing call with
+    # events inside the timed steps.  Only that call's SYRK launch runs on
+    # the stream between its two events, so their sum is the SYRK time
+    # within the step.
+    flush_at = _flushing_calls(h, xs)
+    n_pairs = len(flush_at) + 1  # + the remainder flush inside materialize
+    marks = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_pairs)] for _ in range(args.steps)]
+
+    def step(ev=None):
         h.reset()
-        for X in xs:
-            h.add_batch(X)
+        k = 0
+        for i, X in enumerate(xs):
+            if ev is not None and i in flush_at:
+                ev[k][0].record()
+                h.add_batch(X)
+                ev[k][1].record()
+                k += 1
+            else:
+                h.add_batch(X)
+        if ev is not None:
+            ev[k][0].record()
+            h.flush()
+            ev[k][1].record()
         h.materialize(wl.damp_percent, out=out, want_damp=False)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    launches_per_step = _count_flushes(h, xs) + 1  # SYRK passes + materialize
+    h.sync()  # no device-side wait ran out in the warm-up
+    launches_per_step = n_pairs + 1  # SYRK passes + materialize
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as clk:
+    with Clocks(os.path.join(tempfile.gettempdir(), f"hess_bench_clocks_rank{rank}.csv")) as clk:
         time.sleep(0.3)  # let the sampler start before the timed region
         e0.record()
-        for _ in range(args.steps):
-            step()
+        for k in range(args.steps):
+            step(marks[k])
         e1.record()
         torch.cuda.synchronize()
     barrier(ws)
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, ws)
+    h.sync()  # raises if a device-side wait ran out in the timed steps
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, ws)
     value = job_throughput(flops, ms, ws) / 1e12
-
-    # dominant kernel: the fused SYRK passes, timed with events around every
-    # call that triggered a flush (the GPU stays busy between them)
-    kern = _time_syrk(h, xs, reps=3)
-    syrk_tflops = flops / kern["seconds"] / 1e12
+    syrk_ms = sum(a.elapsed_time(b) for ev in marks for a, b in ev) / args.steps
+    assert syrk_ms <= ms_local * 1.0001, (syrk_ms, ms_local)  # disjoint intervals of the step
+    syrk_tflops = flops / (syrk_ms * 1e-3) / 1e12
+    region_s = ms_local * args.steps * 1e-3
+    # the burst peak for a region shorter than the sustained measurement's
+    # seconds-long loop, the sustained one otherwise
+    peak, peak_name = (bf16_burst, "bf16_tflops (burst)") if region_s < 2.0 else \
+        (bf16_sust, "bf16_tflops_sustained")
+    traffic, traffic_note = syrk_traffic(wl.name) if args.dtype == "bf16" and not args.batches \
+        else (None, "no capture for this configuration")
     e2e = None if args.no_e2e else _e2e(h, wl, xs, d, args)
 
     res = {
@@ -193,15 +254,15 @@ def run_ours(args):
                    "damp_percent": wl.damp_percent, "flops_counted": "N*d*(d+1) (upper triangle)",
                    "l2": "inputs (%.2f GB) larger than L2; no flush" % (n_tok * d * 2 / 1e9),
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": round(syrk_tflops, 2), "peak": bf16_sust,
-                     "unit": "TFLOP/s", "frac": round(syrk_tflops / bf16_sust, 4),
-                     "traffic": (SYRK_DRAM_BYTES_PER_LAUNCH.get(wl.name) if args.dtype == "bf16"
-                                 and not args.batches else None),
-                     "traffic_note": "ncu dram bytes per SYRK launch (profiles/); algorithmic X bytes "
-                                     "per launch %.3g" % (2.0 * n_tok * d / max(1, kern["launches"])),
+        "roofline": {"bound": "tensor", "achieved": round(syrk_tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(syrk_tflops / peak, 4),
+                     "traffic": traffic,
+                     "traffic_note": traffic_note + "; algorithmic X bytes per launch %.4g"
+                                     % (2.0 * n_tok * d / n_pairs),
                      "kernel": "syrk_%s_kernel" % args.dtype,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (cuBLAS bf16, dense)",
-                     "launches_timed": kern["launches"]},
+                     "syrk_ms_per_step": round(syrk_ms, 4), "launches_per_step": n_pairs,
+                     "timing": "CUDA events around each flushing call inside the timed steps",
+                     "peak_source": f"{peak_src} {peak_name}: timed region {region_s:.2f} s"},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
@@ -218,18 +279,17 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _count_flushes(h, xs):
+def _flushing_calls(h, xs):
+    """Indices of the add_batch calls that flush the queue in one step."""
+    from gptq_qqq_calibration_gb300.hessian import hess_pending_batches
     h.reset()
-    n = 0
-    for X in xs:
-        before = len(h._queued)
+    at = set()
+    for i, X in enumerate(xs):
         h.add_batch(X)
-        if len(h._queued) < before + 1:
-            n += 1
-    if h._queued:
-        n += 1
+        if hess_pending_batches(h.handle) == 0:
+            at.add(i)
     h.flush()
-    return n
+    return at
 
 
 def _time_syrk(h, xs, reps=3):
@@ -380,35 +440,117 @@ def _x_large_batch_gram(hbm, bf16_burst):
     return out["large_batch_gram"]
 
 
-def _x_flush_per_call(hbm, bf16_burst):
+def _flush_per_call(name, hbm, n_batches=60):
+    """The ragged stream flushed after every batch (no queue fusion): each
+    call reads its X and read-modify-writes the upper triangle of H."""
     import torch
 
-    from gptq_qqq_calibration_gb300 import Hessian, LocalHessian
+    from gptq_qqq_calibration_gb300 import Hessian
     from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
-    out = {}
-    # the ragged stream flushed after every batch (no queue fusion): each call
-    # reads its X and read-modify-writes the upper triangle of H
-    wl = WORKLOADS["d4096_ragged360_loguniform"].scaled(n_batches=60)
+    wl = WORKLOADS[name].scaled(n_batches=n_batches)
     xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
     h = Hessian(wl.d, flush_tokens=1)
     for X in xs:
         h.add_batch(X)
     torch.cuda.synchronize()
     kern = _time_syrk(h, xs, reps=2)
+    h.sync()
     t = kern["seconds"]
     d = wl.d
     tri = d * (d + 1) // 2
     alg_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 4 * 2  # X once + fp32 upper-triangle RMW per call
-    acc_bytes = 2 * wl.n_tokens * d + len(xs) * tri * 8 * 2  # what this library's (hi, lo) tiles move
-    out["flush_per_call"] = {
-        "workload": wl.name + " (first 60 batches, one flush per batch)",
+    h.close()
+    return {
+        "workload": wl.name + f" (first {n_batches} batches, one flush per batch)",
         "us_per_call": round(t / len(xs) * 1e6, 2), "tflops": round(algo_flops(wl.n_tokens, d) / t / 1e12, 2),
         "roofline": {"bound": "hbm", "achieved": round(alg_bytes / t / 1e9, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(alg_bytes / t / 1e9 / hbm, 4),
                      "bytes_counted": "2*n*d + 8*d(d+1)/2 per call (X once, fp32 upper-triangle read+write)",
-                     "acc_tile_bytes_per_s_GB": round(acc_bytes / t / 1e9, 1)}}
+                     "kernel": "syrk_bf16_kernel"}}
+
+
+def _x_flush_per_call(hbm, bf16_burst):
+    return _flush_per_call("d4096_ragged360_loguniform", hbm)
+
+
+def _x_d2560_ragged360(hbm, bf16_burst, steps=10):
+    """The width-2,560 ragged stream with 1 % outlier channels: the fused
+    queue (reset, 360 adds, materialize per step; TFLOP/s and tokens/s
+    against the burst bf16 peak) and the same stream flushed after every
+    batch (GB/s against HBM)."""
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    wl = WORKLOADS["d2560_ragged360_outlier"]
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    h = Hessian(wl.d)
+    out = torch.empty((wl.d, wl.d), dtype=torch.float32, device="cuda")
+
+    def step():
+        h.reset()
+        for X in xs:
+            h.add_batch(X)
+        h.materialize(wl.damp_percent, out=out, want_damp=False)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    h.sync()
+    t = e0.elapsed_time(e1) * 1e-3 / steps
+    fl = algo_flops(wl.n_tokens, wl.d)
     h.close()
-    return out["flush_per_call"]
+    return {
+        "workload": wl.name, "tokens": wl.n_tokens, "ms_per_step": round(t * 1e3, 3),
+        "tflops": round(fl / t / 1e12, 2), "tokens_per_s": round(wl.n_tokens / t, 1),
+        "roofline": {"bound": "tensor", "peak": bf16_burst, "unit": "TFLOP/s",
+                     "frac": round(fl / t / 1e12 / bf16_burst, 4),
+                     "peak_source": "bf16_tflops (burst)", "timing": "whole step incl. materialize"},
+        "flush_per_call": _flush_per_call(wl.name, hbm)}
+
+
+def _x_d256_latency(hbm, bf16_burst, steps=200):
+    """The single small layer (d = 256, 4 x 128 tokens): latency of one
+    accumulate-and-materialize, on the device (events) and on the host
+    (wall clock of the four add_batch calls and the materialize, which waits
+    for the damping value)."""
+    import torch
+
+    from gptq_qqq_calibration_gb300 import Hessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    wl = WORKLOADS["d256_4x128"]
+    xs = [wl.batch(b, device="cuda") for b in range(len(wl.token_counts))]
+    h = Hessian(wl.d)
+    out = torch.empty((wl.d, wl.d), dtype=torch.float32, device="cuda")
+
+    def step():
+        h.reset()
+        for X in xs:
+            h.add_batch(X)
+        return h.materialize(wl.damp_percent, out=out, want_damp=True)[1]
+    for _ in range(10):
+        step()
+    torch.cuda.synchronize()
+    dev, wall = [], []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        wall.append(time.perf_counter() - t0)
+        dev.append(a.elapsed_time(b) * 1e-3)
+    h.close()
+    return {"workload": wl.name, "device_us_per_step": round(statistics.median(dev) * 1e6, 2),
+            "wall_us_per_step": round(statistics.median(wall) * 1e6, 2),
+            "step": "reset, 4 x add_batch (128 tokens), materialize with the damping value read back",
+            "note": "latency-bound (X 262 KB, H 132 KB): no roofline grade"}
 
 
 def _x_f32_input_ragged(hbm, bf16_burst):
@@ -598,6 +740,8 @@ def _x_merge(hbm, bf16_burst, d=4096, reps=5):
 
 
 EXTRAS = {
+    "d256_latency": _x_d256_latency,
+    "d2560_ragged360": _x_d2560_ragged360,
     "large_batch_gram": _x_large_batch_gram,
     "flush_per_call": _x_flush_per_call,
     "f32_input_ragged": _x_f32_input_ragged,
@@ -635,16 +779,63 @@ def cpu_baseline(wl, budget_s=15.0):
     t_used += time.perf_counter() - t0
     return {"value": round(algo_flops(n_used, wl.d) / t_used / 1e12, 5), "unit": "TFLOP/s",
             "tokens_per_s": round(n_used / t_used, 1), "cores": _blas_threads(), "kind": "oracle",
+            "host_cpus": os.cpu_count(),
             "sample": f"first {nb} of {len(wl.token_counts)} batches ({n_used} tokens) of {wl.name}, "
-                      f"float64 NumPy X^T X + materialize, {t_used:.1f} s"}
+                      f"float64 NumPy X^T X + materialize, {t_used:.1f} s",
+            "one_thread": _oracle_one_thread()}
 
 
 def _blas_threads():
+    """BLAS threads of the oracle: the count set in the environment before
+    numpy loaded (threadpoolctl's report where it is installed)."""
     try:
         from threadpoolctl import threadpool_info
-        return max(i.get("num_threads", 1) for i in threadpool_info())
+        return max(i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas")
     except Exception:
-        return os.cpu_count()
+        return int(os.environ["OPENBLAS_NUM_THREADS"])
+
+
+def _oracle_probe(name):
+    """One oracle timing, in this process (whose BLAS thread count the parent
+    fixed): `d256` is the small layer's 4 x 128 tokens plus materialize;
+    `d4096_update` is one 32,768-token update at d = 4,096."""
+    import torch
+
+    from oracle import GramOracle
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS, make_batch
+    wl = WORKLOADS["d256_4x128" if name == "d256" else "d4096_16x32768"]
+    nb = len(wl.token_counts) if name == "d256" else 1
+    xs = [make_batch(int(n), wl.d, wl.batch_seed(b), profile=wl.profile, profile_seed=wl.seed,
+                     dtype=torch.bfloat16).to(torch.float64).numpy()
+          for b, n in enumerate(wl.token_counts[:nb])]
+    reps = 20 if name == "d256" else 1
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        o = GramOracle(wl.d)
+        for X in xs:
+            o.add_batch(X)
+        o.materialize(wl.damp_percent)
+    dt = (time.perf_counter() - t0) / reps
+    n_tok = sum(x.shape[0] for x in xs)
+    return {"seconds": round(dt, 6), "tokens_per_s": round(n_tok / dt, 1),
+            "tflops": round(algo_flops(n_tok, wl.d) / dt / 1e12, 5), "threads": _blas_threads(),
+            "sample": f"{nb} batch(es), {n_tok} tokens at d={wl.d}, with materialize"}
+
+
+def _oracle_one_thread():
+    """The oracle with one BLAS thread (a child process, so that the thread
+    count is fixed before numpy loads) on the small layer and on one
+    32,768-token update at d = 4,096."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = {}
+    for name in ("d256", "d4096_update"):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-probe", name],
+                           env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, timeout=600)
+        try:
+            out[name] = json.loads(r.stdout.decode().strip().splitlines()[-1])
+        except Exception:
+            out[name] = {"error": r.stderr.decode(errors="replace")[-300:]}
+    return out
 
 
 def run_reference(args):
@@ -705,13 +896,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-batches", type=int, default=2)
     ap.add_argument("--only", default=None,
-                    help="run one secondary measurement (large_batch_gram, flush_per_call, f32_input_ragged, "
-                         "imatrix, local_hessian, merge, quantize_pass) and print its JSON")
+                    help="run one secondary measurement (" + ", ".join(EXTRAS) + ") and print its JSON")
     ap.add_argument("--quantize-only", action="store_true", help="same as --only quantize_pass")
+    ap.add_argument("--oracle-probe", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_probe:
+        print(json.dumps(_oracle_probe(args.oracle_probe)))
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -1,11 +1,13 @@
 """Parity at the full workload sizes, in the launch configuration bench.py
 times (default queue, flush and split-K settings).
 
-d=256 is checked entry by entry against the full float64 oracle.  At widths
-2,560 and 4,096 the oracle computes a seeded sample of 48 whole columns of
-the Gram (every row) plus the full diagonal, which fixes mean(diag H) and
-the damping; the GPU result must match those entries.  The local workload
-is checked block by block in full.
+d=256 and the ragged streams at widths 2,560 and 4,096 (bf16 and fp32
+input) are checked entry by entry against the full float64 oracle.  For the
+large-batch workload (16 x 32,768 tokens at d = 4,096) the oracle computes
+a seeded sample of 48 whole columns of the Gram (every row) plus the full
+diagonal, which fixes mean(diag H) and the damping; the GPU result must
+match those entries.  The local workload is checked block by block in
+full.
 """
 
 import numpy as np
@@ -81,19 +83,48 @@ def _sampled_check(name, n_cols=48, dtype=torch.bfloat16, **opts):
     return err
 
 
-def test_d2560_ragged_outlier_channels():
-    err = _sampled_check("d2560_ragged360_outlier")
+def _full_check(name, dtype=torch.bfloat16, **opts):
+    """The whole d x d Hessian of a workload against the float64 oracle,
+    entry by entry (GPTQModel PR #2981, Validation: the closed form
+    2/N X^T X), in the default queue, flush and split-K settings."""
+    from gptq_qqq_calibration_gb300 import Hessian
+    from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
+    wl = WORKLOADS[name]
+    h = Hessian(wl.d, **opts)
+    o = GramOracle(wl.d)
+    for b in range(len(wl.token_counts)):
+        X = wl.batch(b, device="cuda", dtype=dtype)
+        h.add_batch(X)
+        o.add_batch(host(X))
+    H, damp = h.materialize(wl.damp_percent)
+    h.sync()
+    assert h.n_tokens == o.N == wl.n_tokens
+    Href, dref = o.materialize(wl.damp_percent)
+    Hn = H.cpu().numpy()
+    h.close()
+    mean_diag = float(np.mean(np.diagonal(o.hessian())))
+    err = float(np.abs(Hn.astype(np.float64) - Href).max() / mean_diag)
+    assert np.array_equal(Hn, Hn.T)
+    print(f"\n{name} ({dtype}): max|dH|/mean diag = {err:.3e} over all {wl.d}x{wl.d} entries")
+    return err, damp, dref
+
+
+def test_d2560_ragged_outlier_channels_full():
+    err, damp, dref = _full_check("d2560_ragged360_outlier")
     assert err <= TOL_BF16, err
+    assert damp == pytest.approx(dref, rel=TOL_BF16)
 
 
-def test_d4096_ragged_loguniform_bf16():
-    err = _sampled_check("d4096_ragged360_loguniform")
+def test_d4096_ragged_loguniform_bf16_full():
+    err, damp, dref = _full_check("d4096_ragged360_loguniform")
     assert err <= TOL_BF16, err
+    assert damp == pytest.approx(dref, rel=TOL_BF16)
 
 
-def test_d4096_ragged_loguniform_f32():
-    err = _sampled_check("d4096_ragged360_loguniform", dtype=torch.float32)
+def test_d4096_ragged_loguniform_f32_full():
+    err, damp, dref = _full_check("d4096_ragged360_loguniform", dtype=torch.float32)
     assert err <= TOL_F32, err
+    assert damp == pytest.approx(dref, rel=TOL_F32)
 
 
 def test_d4096_large_batches():
