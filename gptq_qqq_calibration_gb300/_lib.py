@@ -18,7 +18,8 @@ HESS_BF16, HESS_F32 = 0, 1
 STATUS_NAMES = {0: "HESS_OK", 1: "HESS_ERR_INVALID", 2: "HESS_ERR_UNSUPPORTED", 3: "HESS_ERR_OOM",
                 4: "HESS_ERR_CUDA", 5: "HESS_ERR_TIMEOUT", 6: "HESS_ERR_NOT_PD"}
 OPTIONS = {"flush_tokens": 1, "max_pending": 2, "chunk_tokens": 3, "wait_timeout_ns": 4,
-           "split_k": 5, "grid": 6, "pair_kernel": 7}
+           "split_k": 5, "grid": 6, "pair_kernel": 7, "fold_every": 8,
+           "overlap_launches": 9}
 
 _vp, _i32, _i64, _f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
 _fp = ctypes.POINTER(ctypes.c_float)

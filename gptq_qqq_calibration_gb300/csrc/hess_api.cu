@@ -152,6 +152,9 @@ struct hess_ctx {
     int split_k = 0;
     int grid = 0;
     int pair_kernel = 0;  // bf16: 1 = pairs of SMs (256 x 128 tiles), 0 = one SM per tile
+    int fold_every = 8;   // single-slab flushes per kAccPair flush (the others are kAccLo)
+    int overlap = 1;      // launch flushes with programmatic stream serialization
+    int lo_flushes = 0;   // kAccLo flushes since lo was last folded into hi
     int max_pairs = 0;
     hk::SyrkParams* params = nullptr;  // host staging of the launch parameters
 };
@@ -225,6 +228,24 @@ hess_status mark_acc(hess_ctx* h, cudaStream_t s) {
     return HESS_OK;
 }
 
+// Write-back mode of the next flush.  A single-slab flush usually adds to
+// the lo plane alone (kAccLo: 8 bytes per accumulator element instead of
+// 16); every fold_every-th one adds to both planes (kAccPair), which also
+// folds lo back into hi.  lo then never holds more than fold_every - 1
+// undigested flush sums, each added with one fp32 rounding of at most
+// (fold_every - 1) flushes' magnitude: relative to H, unbiased errors of
+// about 2^-24 (fold_every / flushes)^(1/2) per entry.  Split-K flushes add
+// compensated atomics to both planes and leave the count as it is.
+int32_t next_acc_mode(hess_ctx* h, int exclusive) {
+    if (!exclusive) return hk::kAccPair;
+    if (h->lo_flushes + 1 < h->fold_every) {
+        ++h->lo_flushes;
+        return hk::kAccLo;
+    }
+    h->lo_flushes = 0;
+    return hk::kAccPair;
+}
+
 hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     if (h->pending.empty()) return HESS_OK;
     // Order the flush after the work that produced every queued batch.
@@ -280,16 +301,29 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
                                    : choose_slabs(p.n_tiles, p.total_kb, hk::kKBlock, pairs_max);
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
+        p.acc_mode = next_acc_mode(h, p.exclusive);
+        p.tail_split = 0;
         grid = 2 * std::min(pairs_max, p.n_units);
-        e = hk::launch_syrk_bf16_2sm(p, grid, stream);
+        e = hk::launch_syrk_bf16_2sm(p, grid, stream, h->overlap != 0);
     } else {
         const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(h->n_tiles, p.total_kb, kblock, grid_max);
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
+        p.acc_mode = next_acc_mode(h, p.exclusive);
+        // A single-slab flush whose last wave would fill at most half the
+        // grid runs that wave's tiles as two half units each (kAccLo adds
+        // them with reductions in L2, so two writers per tile are fine).
+        const int rem = p.n_tiles % grid_max;
+        p.tail_split = (p.exclusive && p.acc_mode == hk::kAccLo && p.n_tiles > grid_max && rem > 0 &&
+                        2 * rem <= grid_max && p.total_kb >= 2)
+                           ? rem
+                           : 0;
+        p.n_units += p.tail_split;
         grid = std::min(grid_max, p.n_units);
-        e = f32 ? hk::launch_syrk_f32(p, grid, stream) : hk::launch_syrk_bf16(p, grid, stream);
+        e = f32 ? hk::launch_syrk_f32(p, grid, stream, h->overlap != 0)
+                : hk::launch_syrk_bf16(p, grid, stream, h->overlap != 0);
     }
     h->pending.clear();
     h->pending_tokens = 0;
@@ -301,7 +335,8 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     }
     if (std::getenv("HESS_TRACE"))
         std::fprintf(stderr, "[hess] flush d=%lld batches=%d kblocks=%d slabs=%d%s grid=%d %s (max pairs %d)\n",
-                     static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs, p.exclusive ? " (exclusive)" : "", grid,
+                     static_cast<long long>(h->d), nb, p.total_kb, p.n_slabs,
+                     p.exclusive ? (p.acc_mode == hk::kAccLo ? " (exclusive, lo)" : " (exclusive, pair)") : "", grid,
                      f32 ? "f32" : (pairs ? "bf16-pairs" : "bf16"), h->max_pairs);
     return HESS_OK;
 }
@@ -507,6 +542,7 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->pending_tokens = 0;
     h->pending_dtype = -1;
     h->N = 0;
+    h->lo_flushes = 0;
     h->timed_out = false;
     h->status_copy_pending = false;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
@@ -550,6 +586,15 @@ HESS_EXPORT hess_status hess_set_option(hess_t h, int32_t option, int64_t value)
         case HESS_OPT_PAIR_KERNEL:
             if (value != 0 && value != 1) return fail(HESS_ERR_INVALID, "pair_kernel must be 0 or 1");
             h->pair_kernel = static_cast<int>(value);
+            return HESS_OK;
+        case HESS_OPT_OVERLAP_LAUNCHES:
+            if (value != 0 && value != 1) return fail(HESS_ERR_INVALID, "overlap_launches must be 0 or 1");
+            h->overlap = static_cast<int>(value);
+            return HESS_OK;
+        case HESS_OPT_FOLD_EVERY:
+            if (value < 1 || value > 64) return fail(HESS_ERR_INVALID, "fold_every must be in [1, 64]");
+            h->fold_every = static_cast<int>(value);
+            h->lo_flushes = std::min(h->lo_flushes, h->fold_every - 1);
             return HESS_OK;
         default:
             return fail(HESS_ERR_INVALID, "unknown option %d", option);
@@ -602,6 +647,7 @@ HESS_EXPORT hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream)
     CUDA_TRY(hk::launch_add_pairs(dst->acc, src->acc, static_cast<size_t>(dst->n_tiles), dst->sm_count, s));
     if ((st = mark_acc(src, s)) != HESS_OK || (st = mark_acc(dst, s)) != HESS_OK) return st;
     dst->N += src->N;
+    dst->lo_flushes = 0;  // the merge leaves dst's pairs renormalised
     return HESS_OK;
 }
 
@@ -645,15 +691,29 @@ HESS_EXPORT hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream
     h->split_k = src->split_k;
     h->grid = src->grid;
     h->pair_kernel = src->pair_kernel;
+    h->fold_every = src->fold_every;
+    h->overlap = src->overlap;
+    h->lo_flushes = src->lo_flushes;
     *out = h;
     return HESS_OK;
 }
 
 // ------------------------------------------------------ checkpoint / resume
 
+// A state blob is the accumulator tiles followed by a 16-byte trailer:
+// {kStateMagic, HESS_ABI_VERSION, kAccLo flushes not yet folded, 0}.  The
+// trailer is stored by a kernel into the handle's status block (words
+// kTrailerWord..+3) and copied from there, in stream order.
+constexpr uint32_t kStateMagic = 0x48535431u;  // "HST1"
+constexpr int kTrailerWord = 8;
+
+int64_t acc_bytes(const hess_ctx* h) {
+    return static_cast<int64_t>(h->n_tiles) * hk::kTileWords * static_cast<int64_t>(sizeof(float));
+}
+
 HESS_EXPORT int64_t hess_state_bytes(hess_t h) {
     if (!h) return 0;
-    return static_cast<int64_t>(h->n_tiles) * hk::kTileWords * static_cast<int64_t>(sizeof(float));
+    return acc_bytes(h) + 16;
 }
 
 HESS_EXPORT hess_status hess_export_state(hess_t h, void* dst, int64_t bytes, hess_stream_t stream,
@@ -670,7 +730,12 @@ HESS_EXPORT hess_status hess_export_state(hess_t h, void* dst, int64_t bytes, he
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = flush_locked(h, s)) != HESS_OK) return st;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
-    CUDA_TRY(cudaMemcpyAsync(dst, h->acc, static_cast<size_t>(need), cudaMemcpyDefault, s));
+    const size_t ab = static_cast<size_t>(acc_bytes(h));
+    CUDA_TRY(cudaMemcpyAsync(dst, h->acc, ab, cudaMemcpyDefault, s));
+    uint32_t* trailer = h->status + kTrailerWord;
+    CUDA_TRY(hk::launch_store_words(trailer, kStateMagic, HESS_ABI_VERSION,
+                                    static_cast<uint32_t>(h->lo_flushes), 0u, s));
+    CUDA_TRY(cudaMemcpyAsync(static_cast<char*>(dst) + ab, trailer, 16, cudaMemcpyDefault, s));
     if ((st = mark_acc(h, s)) != HESS_OK) return st;
     *n_tokens_out = h->N;
     return HESS_OK;
@@ -689,13 +754,22 @@ HESS_EXPORT hess_status hess_import_state(hess_t h, const void* src, int64_t byt
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the trailer first (the call waits for it): it must name this library
+    const size_t ab = static_cast<size_t>(acc_bytes(h));
+    CUDA_TRY(cudaMemcpyAsync(h->status_host + kTrailerWord, static_cast<const char*>(src) + ab, 16,
+                             cudaMemcpyDefault, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    const volatile uint32_t* tr = h->status_host + kTrailerWord;
+    if (tr[0] != kStateMagic || tr[1] != HESS_ABI_VERSION || tr[2] > 64u)
+        return fail(HESS_ERR_INVALID, "src is not a state blob of this library version");
     h->pending.clear();
     h->pending_tokens = 0;
     h->pending_dtype = -1;
     h->timed_out = false;
     h->status_copy_pending = false;
+    h->lo_flushes = std::min(static_cast<int>(tr[2]), h->fold_every - 1);
     if ((st = order_acc(h, s)) != HESS_OK) return st;
-    CUDA_TRY(cudaMemcpyAsync(h->acc, src, static_cast<size_t>(need), cudaMemcpyDefault, s));
+    CUDA_TRY(cudaMemcpyAsync(h->acc, src, ab, cudaMemcpyDefault, s));
     CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
     h->N = n_tokens;
     return mark_acc(h, s);

@@ -47,6 +47,17 @@ constexpr uint32_t kStatusTimeoutMma = 2u;
 constexpr uint32_t kStatusTimeoutEpilogue = 4u;
 constexpr uint32_t kStatusTimeoutDrain = 8u;
 
+// How an exclusive (single-slab) launch adds a unit's compensated sum
+// (hi', lo') to its accumulator tile.  kAccPair renormalises the stored pair
+// and adds exactly: (hi, lo) <- TwoSum(hi, lo) + (hi', lo').  kAccLo touches
+// only the lo plane, lo <- lo + (hi' + lo') rounded to nearest, which halves
+// the accumulator bytes a launch moves; lo then holds the last few launches'
+// sums undigested (hi + lo stays the value) until the next kAccPair launch
+// folds it back.  Every reader of the accumulator takes hi + lo, so both
+// states are valid inputs everywhere.
+constexpr int32_t kAccPair = 0;
+constexpr int32_t kAccLo = 1;
+
 // One fused split-K pass over the queued batches of one dtype.
 struct SyrkParams {
     CUtensorMap maps[kMaxBatches];      // batch b: dims {d, n_b}, 128B swizzle
@@ -61,6 +72,11 @@ struct SyrkParams {
     int32_t n_units;        // n_tiles * n_slabs
     int32_t exclusive;      // 1: one token slab, so each accumulator tile has one writer and the
                             // epilogue reads, adds and stores it (else compensated atomics)
+    int32_t acc_mode;       // exclusive launches: kAccPair or kAccLo
+    int32_t tail_split;     // single-slab kAccLo launches: the last tail_split tiles of the tile
+                            // order run as two units of half the k-blocks each (their lo sums
+                            // meet in L2), so that the last wave of units is as short as the rest
+                            // allow; n_units = n_tiles + tail_split
     float* acc;             // (hi, lo) accumulator (tile layout above)
     uint32_t* status;
     unsigned long long timeout_ns;
@@ -72,12 +88,16 @@ __host__ __device__ inline int tile_index(int I, int J, int T) {
 }
 
 cudaError_t syrk_bf16_prepare();  // sets the dynamic shared-memory limit (per device)
-cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s);
+// `overlap`: launch with programmatic stream serialization, so that the
+// kernel's set-up may run while the previous kernel of the stream ends (every
+// SYRK kernel waits for the previous grid before it reads X or the
+// accumulator).
+cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s, bool overlap);
 
 // Pair-of-SMs bf16 kernel (256 x 128 tiles): n_tiles counts pair tiles,
 // sum over I2 < ceil(T/2) of (T - 2*I2); the grid is 2 CTAs per pair.
 cudaError_t syrk_bf16_2sm_prepare(int* max_pairs);
-cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s);
+cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s, bool overlap);
 __host__ __device__ inline int pair_tile_count(int T) {
     int n = 0;
     for (int i = 0; 2 * i < T; ++i) n += T - 2 * i;
@@ -109,7 +129,7 @@ cudaError_t launch_gemm_tf32(const float* P, int ldp, const float* Q, int ldq, f
                              cudaStream_t s, bool lower = false);
 
 cudaError_t syrk_f32_prepare();
-cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s);
+cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s, bool overlap);
 
 // Materialize: damp = damp_percent * mean_i(acc_ii * scale) into damp_out
 // (fp64) and damp_out_f32; then H_out (row-major d x d fp32).
@@ -137,6 +157,10 @@ cudaError_t local_prepare();
 cudaError_t launch_local_gram(const LocalParams& p, int grid, cudaStream_t s);
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
                               cudaStream_t s);
+
+// Four 32-bit words stored to 16-byte-aligned device memory, in stream order.
+cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                               cudaStream_t s);
 
 // dst += src over n_tiles (hi, lo) accumulator tiles (accumulator merge).
 cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int sm_count,

@@ -10,11 +10,13 @@
 //
 // Readings: the mean of the diagonal is taken of the scaled matrix, in
 // fp64; diagonal elements are computed in fp64 and rounded once to fp32;
-// off-diagonal elements (hi + lo) * scale are computed in fp32 with an exact
-// product (FMA) and rounded to within an ulp of the correctly rounded value;
+// off-diagonal elements (hi + lo) * scale are computed in fp32 (the pair
+// renormalised with an exact TwoSum, then an exact product by FMA) and
+// rounded to within an ulp of the correctly rounded value;
 // H_out[j][i] is a copy of H_out[i][j] (i <= j) so the result is exactly
 // symmetric.
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace hk {
 namespace {
@@ -81,11 +83,16 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int c = c0 + 4 * q + m;
+            // The stored pair may be unnormalised (the low part can hold
+            // recent flushes' sums that nearly cancel the high part), so it
+            // is first renormalised exactly: h = RN(hi + lo), l the error.
+            float l;
+            const float h = two_sum_f32(hs[m], ls[m], l);
             // (h + l) * (scale_hi + scale_lo): the exact product h * scale_hi
             // as p + pe, plus the small cross terms, then one rounding
-            const float p = __fmul_rn(hs[m], scale_hi);
-            const float pe = __fmaf_rn(hs[m], scale_hi, -p);
-            const float cross = __fmaf_rn(ls[m], scale_hi, __fmaf_rn(hs[m], scale_lo, pe));
+            const float p = __fmul_rn(h, scale_hi);
+            const float pe = __fmaf_rn(h, scale_hi, -p);
+            const float cross = __fmaf_rn(l, scale_hi, __fmaf_rn(h, scale_lo, pe));
             const float v = __fadd_rn(p, cross);
             tr[4 * q + m][tx] = v;
             if (r < c && c < d) H[static_cast<size_t>(c) * d + r] = v;

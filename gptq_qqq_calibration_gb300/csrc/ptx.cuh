@@ -76,6 +76,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 
 // 2-D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes.  x is the innermost (contiguous) coordinate.
+// Fetches a tensor map (kernel parameter or global) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {
     asm volatile(
@@ -216,6 +221,39 @@ __device__ __forceinline__ uint64_t two_sum2(uint64_t a, uint64_t b, uint64_t& e
     const uint64_t bb = sub2(s, a);
     err = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
     return s;
+}
+
+// ------------------------------------------ programmatic dependent launch
+
+// Lets the next kernel of the stream, if it was launched with programmatic
+// stream serialization, be scheduled before this grid ends (on SMs this grid
+// no longer uses).  No effect otherwise.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible.  Returns at once when the grid was launched in
+// plain stream order.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------- L2 policies
+
+// An L2 cache policy that keeps the lines it tags ahead of other lines when
+// L2 must evict (for data reused by the next launch).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void red_add_v4_f32_hint(float* p, float4 v, uint64_t pol) {
+    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_bulk_hint(const void* ptr, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes),
+                 "l"(pol)
+                 : "memory");
 }
 
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.

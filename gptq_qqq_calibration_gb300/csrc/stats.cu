@@ -20,10 +20,11 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
     return s;
 }
 
-// dst += src over (hi, lo) accumulator tiles: per element, TwoSum of the hi
-// parts, the lo parts and the error added, and the pair renormalised with
-// Fast2Sum.  Four elements per thread (float4 of each plane), grid-stride
-// over the tiles' planes.
+// dst += src over (hi, lo) accumulator tiles.  Per element, each stored pair
+// is first renormalised with an exact TwoSum (its lo may hold undigested
+// flush sums), then: TwoSum of the hi parts, the lo parts and the error
+// added, and the pair renormalised with Fast2Sum.  Four elements per thread
+// (float4 of each plane), grid-stride over the tiles' planes.
 __global__ void __launch_bounds__(256) add_pairs_kernel(float* __restrict__ dst,
                                                         const float* __restrict__ src,
                                                         size_t n_tiles) {
@@ -44,9 +45,11 @@ __global__ void __launch_bounds__(256) add_pairs_kernel(float* __restrict__ dst,
         const float b_l[4] = {bl.x, bl.y, bl.z, bl.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float e;
-            const float s = two_sum(*a_h[i], b_h[i], e);
-            const float l = __fadd_rn(__fadd_rn(*a_l[i], b_l[i]), e);
+            float fa, fb, e;
+            const float ha = two_sum(*a_h[i], *a_l[i], fa);
+            const float hb = two_sum(b_h[i], b_l[i], fb);
+            const float s = two_sum(ha, hb, e);
+            const float l = __fadd_rn(__fadd_rn(fa, fb), e);
             const float hi = __fadd_rn(s, l);
             *a_h[i] = hi;
             *a_l[i] = __fsub_rn(l, __fsub_rn(hi, s));  // Fast2Sum error (|s| >= |l|)
@@ -141,6 +144,16 @@ cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int s
     const size_t want = (n_tiles * (kTileElems / 4) + 255) / 256;
     const int grid = static_cast<int>(want < static_cast<size_t>(4 * sm_count) ? want : 4 * sm_count);
     add_pairs_kernel<<<grid, 256, 0, s>>>(dst, src, n_tiles);
+    return cudaGetLastError();
+}
+
+namespace {
+__global__ void store_words_kernel(uint4* dst, uint4 v) { *dst = v; }
+}  // namespace
+
+cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                               cudaStream_t s) {
+    store_words_kernel<<<1, 1, 0, s>>>(reinterpret_cast<uint4*>(dst), make_uint4(w0, w1, w2, w3));
     return cudaGetLastError();
 }
 

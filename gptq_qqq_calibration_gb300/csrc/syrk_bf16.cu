@@ -101,6 +101,13 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // Set-up above may overlap the end of the previous kernel of the stream
+    // (programmatic dependent launch); X and the accumulator are read only
+    // after it has completed, and before any bounded wait starts.  The next
+    // flush of the stream may then start on the SMs this grid leaves.
+    if (threadIdx.x == 0) syrk::prefetch_first_map(p);
+    griddep_wait();
+    griddep_launch_dependents();
     const unsigned long long limit = p.timeout_ns;
     if (warp < kFirstEpiWarp) {
       setmaxnreg_dec<kRegsLow>();
@@ -253,12 +260,9 @@ cudaError_t syrk_bf16_prepare() {
     return cudaSuccess;
 }
 
-cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s) {
-    if (p.exclusive)
-        syrk_bf16_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
-    else
-        syrk_bf16_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_syrk_bf16(const SyrkParams& p, int grid, cudaStream_t s, bool overlap) {
+    return syrk::launch_syrk(p.exclusive ? syrk_bf16_kernel<true> : syrk_bf16_kernel<false>, p, grid, kThreads,
+                             kSmemBytes, s, overlap);
 }
 
 }  // namespace hk

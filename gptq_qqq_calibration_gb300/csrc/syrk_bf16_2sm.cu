@@ -123,6 +123,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // Set-up above may overlap the end of the previous kernel of the stream
+    // (programmatic dependent launch); X and the accumulator are read only
+    // after it has completed, and before any bounded wait starts.  The next
+    // flush of the stream may then start on the SMs this grid leaves.
+    griddep_wait();
+    griddep_launch_dependents();
     const unsigned long long limit = p.timeout_ns;
 
     if (warp < kFirstEpiWarp) {
@@ -296,12 +302,9 @@ cudaError_t syrk_bf16_2sm_prepare(int* max_pairs) {
     return cudaSuccess;
 }
 
-cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s) {
-    if (p.exclusive)
-        syrk_bf16_2sm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
-    else
-        syrk_bf16_2sm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_syrk_bf16_2sm(const SyrkParams& p, int grid, cudaStream_t s, bool overlap) {
+    return syrk::launch_syrk(p.exclusive ? syrk_bf16_2sm_kernel<true> : syrk_bf16_2sm_kernel<false>, p, grid, kThreads,
+                             kSmemBytes, s, overlap);
 }
 
 }  // namespace hk

@@ -15,9 +15,30 @@ struct Unit {
     int t, I, J, k0, k1;
 };
 
+// With p.tail_split > 0 (one slab): units below n_tiles - tail_split are
+// whole tiles; the rest are the last tail_split tiles, each as its first and
+// second half of the k-blocks.
 __device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
-    const int slab = u / p.n_tiles;
-    const int t = u - slab * p.n_tiles;
+    int t;
+    if (p.tail_split > 0) {
+        const int whole = p.n_tiles - p.tail_split;
+        if (u < whole) {
+            t = u;
+            un.k0 = 0;
+            un.k1 = p.total_kb;
+        } else {
+            const int v = u - whole;
+            t = whole + (v >> 1);
+            const int mid = p.total_kb >> 1;
+            un.k0 = (v & 1) ? mid : 0;
+            un.k1 = (v & 1) ? p.total_kb : mid;
+        }
+    } else {
+        const int slab = u / p.n_tiles;
+        t = u - slab * p.n_tiles;
+        un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
+        un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
+    }
     int i = 0, rem = t;
     while (rem >= p.tiles_per_dim - i) {
         rem -= p.tiles_per_dim - i;
@@ -26,9 +47,19 @@ __device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
     un.t = t;
     un.I = i;
     un.J = i + rem;
-    un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
-    un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
     return un.k1 > un.k0;
+}
+
+// Before the wait for the previous grid (which reads nothing of the
+// previous kernel's output): the first unit's tensor map is fetched into
+// the descriptor cache and the parameters into the constant cache.
+__device__ __forceinline__ void prefetch_first_map(const SyrkParams& p) {
+    Unit un;
+    if (static_cast<int>(blockIdx.x) < p.n_units && unit_at(p, blockIdx.x, un)) {
+        int b = 0;
+        while (p.kb_start[b + 1] <= un.k0) ++b;
+        prefetch_tensormap(&p.maps[b]);
+    }
 }
 
 constexpr int kEpiWarps = 8;                   // 2 per tensor-memory lane quarter
@@ -52,7 +83,8 @@ constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 // At the end of a unit, (hi, lo) is added to the (hi, lo) accumulator tile
 // `out_tile` (skipped when it is negative): by a plain read-modify-write when
 // the launch has one token slab (kExcl, the kernel instance chosen when
-// p.exclusive is set), else by compensated fp32 atomics.
+// p.exclusive is set) -- of both planes (kAccPair) or of the lo plane alone
+// (kAccLo) -- else by compensated fp32 atomics.
 //   unit_fn(u, k0, k1, out_tile) -> false if unit u is empty;
 //   wait_full(bar, parity) waits for a filled accumulator buffer;
 //   arrive_empty(b) releases buffer b to the MMA issuer.
@@ -75,9 +107,14 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         if (!unit_fn(u, k0, k1, out_tile)) continue;
         if constexpr (kExcl) {
             // the tile's old values travel to L2 while the unit's MMAs run
-            if (out_tile >= 0 && warp == first_warp && lane == 0)
-                prefetch_l2_bulk(p.acc + static_cast<size_t>(out_tile) * kTileWords,
-                                 kTileWords * sizeof(float));
+            if (out_tile >= 0 && warp == first_warp && lane == 0) {
+                if (p.acc_mode == kAccLo)
+                    prefetch_l2_bulk_hint(p.acc + static_cast<size_t>(out_tile) * kTileWords + kTileElems,
+                                          kTileElems * sizeof(float), l2_policy_evict_last());
+                else
+                    prefetch_l2_bulk(p.acc + static_cast<size_t>(out_tile) * kTileWords,
+                                     kTileWords * sizeof(float));
+            }
         }
         const int nch = (k1 - k0 + p.chunk_kb - 1) / p.chunk_kb;
         if constexpr (kGroup > 0) {
@@ -143,10 +180,28 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         // blocks of 4 words); the lo plane is kTileElems further
         float* const out = p.acc + static_cast<size_t>(out_tile) * kTileWords + tile_offset(row, col0);
         if constexpr (kExcl) {
+          if (p.acc_mode == kAccLo) {
+            // Sole writer, lo plane only: lo += hi' + lo', with the add done
+            // in L2 by vector reductions (round to nearest, like an fp32
+            // add): nothing comes back to the SM, so the epilogue moves on
+            // to the next unit at once.
+            // The lo plane is kept in L2 ahead of other lines: the next small
+            // flush reads and adds to the same tiles.
+            const uint64_t pol = l2_policy_evict_last();
+#pragma unroll
+            for (int q = 0; q < kEpiCols / 4; ++q) {
+                float4 v;
+                unpack2(add2(hi[2 * q], lo[2 * q]), v.x, v.y);
+                unpack2(add2(hi[2 * q + 1], lo[2 * q + 1]), v.z, v.w);
+                red_add_v4_f32_hint(out + kTileElems + q * 4 * kTile, v, pol);
+            }
+          } else {
             // Sole writer of this tile in this launch: a plain read-modify-
-            // write of (hi, lo) += (hi', lo') with an exact TwoSum on the hi
-            // parts, 16-byte accesses, kRmw columns' loads in flight at a time
-            // (with kGroup > 0 the dead `mid` registers hold them).
+            // write of (hi, lo) += (hi', lo'), 16-byte accesses, kRmw
+            // columns' loads in flight at a time (with kGroup > 0 the dead
+            // `mid` registers hold them).  The stored pair is renormalised
+            // first with an exact TwoSum (lo may hold undigested kAccLo
+            // sums), then the hi parts are added with an exact TwoSum.
             constexpr int kRmw = kGroup > 0 ? 32 : 8;
 #pragma unroll
             for (int g = 0; g < kEpiCols / kRmw; ++g) {
@@ -160,11 +215,15 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
 #pragma unroll
                 for (int i = 0; i < kRmw / 4; ++i) {
                     const int q = (kRmw * g) / 4 + i;
-                    uint64_t e0, e1;
-                    const uint64_t s0 = two_sum2(pack2(__float_as_uint(oh[i].x), __float_as_uint(oh[i].y)), hi[2 * q], e0);
-                    const uint64_t s1 = two_sum2(pack2(__float_as_uint(oh[i].z), __float_as_uint(oh[i].w)), hi[2 * q + 1], e1);
-                    const uint64_t t0 = add2(add2(pack2(__float_as_uint(ol[i].x), __float_as_uint(ol[i].y)), lo[2 * q]), e0);
-                    const uint64_t t1 = add2(add2(pack2(__float_as_uint(ol[i].z), __float_as_uint(ol[i].w)), lo[2 * q + 1]), e1);
+                    uint64_t f0, f1, e0, e1;
+                    const uint64_t h0 = two_sum2(pack2(__float_as_uint(oh[i].x), __float_as_uint(oh[i].y)),
+                                                 pack2(__float_as_uint(ol[i].x), __float_as_uint(ol[i].y)), f0);
+                    const uint64_t h1 = two_sum2(pack2(__float_as_uint(oh[i].z), __float_as_uint(oh[i].w)),
+                                                 pack2(__float_as_uint(ol[i].z), __float_as_uint(ol[i].w)), f1);
+                    const uint64_t s0 = two_sum2(h0, hi[2 * q], e0);
+                    const uint64_t s1 = two_sum2(h1, hi[2 * q + 1], e1);
+                    const uint64_t t0 = add2(add2(f0, lo[2 * q]), e0);
+                    const uint64_t t1 = add2(add2(f1, lo[2 * q + 1]), e1);
                     float4 nh, nl;
                     unpack2(s0, nh.x, nh.y);
                     unpack2(s1, nh.z, nh.w);
@@ -174,6 +233,7 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
                     *reinterpret_cast<float4*>(out + kTileElems + q * 4 * kTile) = nl;
                 }
             }
+          }
         } else {
             // Several slabs add to this tile: an atomic add of hi' to hi
             // returns the old value, from which the exact rounding error of
@@ -213,6 +273,28 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         }
     }
     if (!ok && lane == 0) atomicOr(p.status, kStatusTimeoutEpilogue);
+}
+
+// Launches a SYRK kernel.  With `overlap`, the launch allows programmatic
+// dependent launch: its CTAs may start on SMs that the previous kernel of the
+// stream has released, before that kernel ends.  Every SYRK kernel does its
+// set-up (barriers, tensor memory), then waits for the previous grid
+// (griddep_wait) before anything else, and lets its own dependents start
+// (griddep_launch_dependents).
+template <class Kernel>
+inline cudaError_t launch_syrk(Kernel kernel, const SyrkParams& p, int grid, int threads, size_t smem,
+                               cudaStream_t s, bool overlap) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 // The single-CTA form: units in blockIdx.x + k * gridDim.x order, local barriers.

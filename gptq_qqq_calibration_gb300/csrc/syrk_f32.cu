@@ -155,6 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    // Set-up above may overlap the end of the previous kernel of the stream
+    // (programmatic dependent launch); X and the accumulator are read only
+    // after it has completed, and before any bounded wait starts.  The next
+    // flush of the stream may then start on the SMs this grid leaves.
+    if (threadIdx.x == 0) syrk::prefetch_first_map(p);
+    griddep_wait();
+    griddep_launch_dependents();
     const unsigned long long limit = p.timeout_ns;
 
     // Converter `ci` (0..kCvtWarps-1) splits its rounds of landed stage
@@ -376,12 +383,9 @@ cudaError_t syrk_f32_prepare() {
     return cudaSuccess;
 }
 
-cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s) {
-    if (p.exclusive)
-        syrk_f32_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
-    else
-        syrk_f32_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s, bool overlap) {
+    return syrk::launch_syrk(p.exclusive ? syrk_f32_kernel<true> : syrk_f32_kernel<false>, p, grid, kThreads,
+                             kSmemBytes, s, overlap);
 }
 
 }  // namespace hk

@@ -36,8 +36,10 @@ _DTYPES = {torch.bfloat16: HESS_BF16, torch.float32: HESS_F32}
 
 
 def _stream(stream: Optional[torch.cuda.Stream]) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    # the raw handle of the current stream, without building a Stream object
+    return torch._C._cuda_getCurrentRawStream(torch.cuda.current_device())
 
 
 def _tokens_view(X: torch.Tensor, d: int) -> tuple:

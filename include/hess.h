@@ -88,9 +88,20 @@ typedef enum {
                                      any wait that is not already satisfied give up) */
     HESS_OPT_SPLIT_K = 5,         /* token slabs per flush; 0 = automatic (default) */
     HESS_OPT_GRID = 6,            /* persistent CTAs per flush; 0 = one per SM (default) */
-    HESS_OPT_PAIR_KERNEL = 7      /* bf16: 0 = tiles of 128x128, one SM each (default),
+    HESS_OPT_PAIR_KERNEL = 7,     /* bf16: 0 = tiles of 128x128, one SM each (default),
                                      1 = tiles of 256x128 on pairs of SMs (fewer operand
                                      bytes per SM; faster with long chunks) */
+    HESS_OPT_FOLD_EVERY = 8,      /* 1..64, default 8: of this many single-slab flushes, one
+                                     updates both fp32 parts of the accumulator and the others
+                                     only its low part, which halves the accumulator bytes a
+                                     small flush moves; the low part holds at most this many
+                                     minus one flushes' sums between folds.  1 = every flush
+                                     updates both parts. */
+    HESS_OPT_OVERLAP_LAUNCHES = 9 /* 1 (default): a flush's kernel is launched so that it may
+                                     be scheduled while the kernel before it in the stream
+                                     ends (programmatic dependent launch); it sets itself up
+                                     there and waits for that kernel's memory before reading
+                                     X or the accumulator.  0: plain stream order. */
 } hess_option;
 
 /* ------------------------------------------------------------------------ */
@@ -156,10 +167,10 @@ hess_status hess_flush(hess_t h, hess_stream_t stream);
  * call after it, until hess_reset or hess_import_state.  hess_sync reports
  * it at once.
  * Errors: INVALID (also for H_out that is not device memory of the
- * handle's device or managed memory), CUDA, TIMEOUT (above).  Every other entry point that takes a device buffer (imatrix_add,
- * imatrix_read, local_hess_add, local_hess_read,
- * local_hess_compute_noalloc, and the gptq_* calls) refuses host memory the
- * same way, before any launch. */
+ * handle's device or managed memory), CUDA, TIMEOUT (above).  Every other
+ * entry point that takes a device buffer (imatrix_add, imatrix_read,
+ * local_hess_add, local_hess_read, local_hess_compute_noalloc, and the
+ * gptq_* calls) refuses host memory the same way, before any launch. */
 hess_status hess_materialize(hess_t h, float* H_out, double damp_percent, hess_stream_t stream,
                              float* damp_value_out);
 
@@ -205,8 +216,11 @@ hess_status hess_clone(hess_t src, hess_t* out, hess_stream_t stream);
  * long calibration run also wants to save its partial Gram and token count
  * and resume later, so these calls have no counterpart on the pages.
  * The state is the accumulator in the library's own layout: an opaque blob of
- * hess_state_bytes(h) bytes, valid for a handle of the same width d and a
- * library of the same HESS_ABI_VERSION. */
+ * hess_state_bytes(h) bytes (the accumulator, then 16 bytes that name the
+ * library version and how far the low parts have been folded), valid for a
+ * handle of the same width d and a library of the same HESS_ABI_VERSION.
+ * A run exported and resumed gives bit for bit the H of the same run
+ * uninterrupted. */
 int64_t hess_state_bytes(hess_t h);  /* 0 for a NULL handle */
 
 /* Flush, then copy the state to `dst` (host or device memory, `bytes` >=
@@ -219,8 +233,9 @@ hess_status hess_export_state(hess_t h, void* dst, int64_t bytes, hess_stream_t 
 
 /* Replace the handle's state by a blob from hess_export_state and set N to
  * n_tokens.  Batches still queued are dropped (as by hess_reset); `src` is
- * read on `stream`.  Errors: INVALID (NULL, bytes != hess_state_bytes(h),
- * n_tokens < 0), CUDA. */
+ * read on `stream`, and the call waits for its trailer.  Errors: INVALID
+ * (NULL, bytes != hess_state_bytes(h), n_tokens < 0, a trailer that does
+ * not name this library version), CUDA. */
 hess_status hess_import_state(hess_t h, const void* src, int64_t bytes, int64_t n_tokens,
                               hess_stream_t stream);
 

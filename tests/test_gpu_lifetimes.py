@@ -33,27 +33,31 @@ def test_clone_while_another_thread_adds():
     that its N names."""
     from gptq_qqq_calibration_gb300 import Hessian
     d = 256
-    counts = np.random.default_rng(31).integers(1, 400, size=160)
+    counts = np.random.default_rng(31).integers(1, 200, size=800)
     xs = list(batches(d, counts, seed=31))
     torch.cuda.synchronize()
     src = Hessian(d, flush_tokens=3000)
     clones = []
-    started = threading.Event()
+    # Clone j runs while the adder adds batches 50 j .. 50 j + 49; the adder
+    # then waits for it, so the clones land at different points of the stream.
+    n_clones = 15
+    done = [threading.Event() for _ in range(n_clones)]
 
     def adder():
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
             for k, X in enumerate(xs):
                 src.add_batch(X, stream=s)
-                if k == 5:
-                    started.set()
+                j = k // 50
+                if k % 50 == 49 and j < n_clones:
+                    done[j].wait(60)
 
     def cloner():
         s = torch.cuda.Stream()
-        started.wait(30)
         with torch.cuda.stream(s):
-            for _ in range(16):
+            for j in range(n_clones):
                 clones.append(src.clone(stream=s))
+                done[j].set()
 
     ta, tc = threading.Thread(target=adder), threading.Thread(target=cloner)
     ta.start()
@@ -69,7 +73,7 @@ def test_clone_while_another_thread_adds():
         k = int(np.searchsorted(prefix, c.n_tokens))
         assert prefix[k] == c.n_tokens, "a clone's N must end on a batch boundary"
         want.setdefault(k, []).append(c)
-    assert len(want) >= 2, "the clones should see several prefixes of the stream"
+    assert len(want) >= 4, f"the clones should see several prefixes of the stream: {sorted(want)}"
     o = GramOracle(d)
     done = 0
     for k in sorted(want):

@@ -83,48 +83,63 @@ def _sampled_check(name, n_cols=48, dtype=torch.bfloat16, **opts):
     return err
 
 
-def _full_check(name, dtype=torch.bfloat16, **opts):
+def _full_check(name, dtype=torch.bfloat16, variants=({},)):
     """The whole d x d Hessian of a workload against the float64 oracle,
     entry by entry (GPTQModel PR #2981, Validation: the closed form
-    2/N X^T X), in the default queue, flush and split-K settings."""
+    2/N X^T X), for one handle per option set in `variants` fed the same
+    batches; {} is the default queue, flush and split-K settings (the
+    launch configuration bench.py times).  Returns [(err, damp)] per
+    variant and the oracle's damping value."""
     from gptq_qqq_calibration_gb300 import Hessian
     from gptq_qqq_calibration_gb300.synthetic import WORKLOADS
     wl = WORKLOADS[name]
-    h = Hessian(wl.d, **opts)
+    hs = [Hessian(wl.d, **v) for v in variants]
     o = GramOracle(wl.d)
     for b in range(len(wl.token_counts)):
         X = wl.batch(b, device="cuda", dtype=dtype)
-        h.add_batch(X)
+        for h in hs:
+            h.add_batch(X)
         o.add_batch(host(X))
-    H, damp = h.materialize(wl.damp_percent)
-    h.sync()
-    assert h.n_tokens == o.N == wl.n_tokens
     Href, dref = o.materialize(wl.damp_percent)
-    Hn = H.cpu().numpy()
-    h.close()
     mean_diag = float(np.mean(np.diagonal(o.hessian())))
-    err = float(np.abs(Hn.astype(np.float64) - Href).max() / mean_diag)
-    assert np.array_equal(Hn, Hn.T)
-    print(f"\n{name} ({dtype}): max|dH|/mean diag = {err:.3e} over all {wl.d}x{wl.d} entries")
-    return err, damp, dref
+    out = []
+    for v, h in zip(variants, hs):
+        H, damp = h.materialize(wl.damp_percent)
+        h.sync()
+        assert h.n_tokens == o.N == wl.n_tokens
+        Hn = H.cpu().numpy()
+        h.close()
+        err = float(np.abs(Hn.astype(np.float64) - Href).max() / mean_diag)
+        assert np.array_equal(Hn, Hn.T)
+        print(f"\n{name} ({dtype}, options {v or 'default'}): max|dH|/mean diag = {err:.3e} "
+              f"over all {wl.d}x{wl.d} entries")
+        out.append((err, damp))
+    return out, dref
 
 
 def test_d2560_ragged_outlier_channels_full():
-    err, damp, dref = _full_check("d2560_ragged360_outlier")
-    assert err <= TOL_BF16, err
-    assert damp == pytest.approx(dref, rel=TOL_BF16)
+    """Fused queue (default) and the same stream flushed after every batch,
+    whose single-slab flushes mostly update the accumulator's low part
+    alone (folded every 8th flush)."""
+    res, dref = _full_check("d2560_ragged360_outlier", variants=({}, {"flush_tokens": 1}))
+    for err, damp in res:
+        assert err <= TOL_BF16, err
+        assert damp == pytest.approx(dref, rel=TOL_BF16)
 
 
 def test_d4096_ragged_loguniform_bf16_full():
-    err, damp, dref = _full_check("d4096_ragged360_loguniform")
-    assert err <= TOL_BF16, err
-    assert damp == pytest.approx(dref, rel=TOL_BF16)
+    (res,), dref = _full_check("d4096_ragged360_loguniform")
+    assert res[0] <= TOL_BF16, res[0]
+    assert res[1] == pytest.approx(dref, rel=TOL_BF16)
 
 
 def test_d4096_ragged_loguniform_f32_full():
-    err, damp, dref = _full_check("d4096_ragged360_loguniform", dtype=torch.float32)
-    assert err <= TOL_F32, err
-    assert damp == pytest.approx(dref, rel=TOL_F32)
+    """fp32 input, fused queue and flushed after every batch."""
+    res, dref = _full_check("d4096_ragged360_loguniform", dtype=torch.float32,
+                            variants=({}, {"flush_tokens": 1}))
+    for err, damp in res:
+        assert err <= TOL_F32, err
+        assert damp == pytest.approx(dref, rel=TOL_F32)
 
 
 def test_d4096_large_batches():
