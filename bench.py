@@ -379,26 +379,31 @@ def _e2e(h, wl, xs, d, args, chunk_bytes=64 << 20):
         torch.cuda.synchronize()
         link.append(total * row_bytes / (a.elapsed_time(b) * 1e-3) / 1e9)
     steps = max(3, args.steps // 2)
-    # each step ends with a device -> host read that the next step's copies
-    # wait for anyway, so timing steps one by one costs nothing; it shows the
-    # host link's occasional stalls (100-160 ms, seen also with the copies
-    # alone) that a mean over the steps absorbs
-    per = []
-    for _ in range(steps):
-        t0 = time.perf_counter()
+    # The steps run back to back, as a calibration loop streams its batches:
+    # each step's copies wait for the previous step's kernels (copy_s waits
+    # on comp), and one synchronisation ends the timed region.  An event
+    # after each step's device -> host read gives the per-step device
+    # intervals.
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ends[0].record(comp)
+    for k in range(steps):
         step()
-        torch.cuda.synchronize()
-        per.append(time.perf_counter() - t0)
-    dt = sum(per) / steps
+        ends[k + 1].record(comp)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    per = [ends[k].elapsed_time(ends[k + 1]) * 1e-3 for k in range(steps)]
     med = statistics.median(per)
     return {"value": round(flops / dt / 1e12, 3), "unit": "TFLOP/s",
             "median_step_ms": round(med * 1e3, 3), "median_tflops": round(flops / med / 1e12, 3),
             "stalled_steps": int(sum(t > 2 * med for t in per)),
+            "longest_step_ms": round(max(per) * 1e3, 3),
             "h2d_link_gbs": round(max(link), 1),
             "h2d_bytes_per_step": int(total * row_bytes),
             "d2h_bytes_per_step": int(d * d * 4), "ms_per_step": round(dt * 1e3, 3),
             "h2d": f"one pinned buffer, {len(chunks)} chunks of ~{chunk_bytes >> 20} MB on a copy stream, "
-                   "overlapped with the flushes"}
+                   "overlapped with the flushes; steps back to back, wall clock over all of them"}
 
 
 # Secondary measurements, each with its own roofline; `--only NAME` runs one.

@@ -236,26 +236,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // plain stream order.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ---------------------------------------------------------- L2 policies
-
-// An L2 cache policy that keeps the lines it tags ahead of other lines when
-// L2 must evict (for data reused by the next launch).
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void red_add_v4_f32_hint(float* p, float4 v, uint64_t pol) {
-    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
-                 : "memory");
-}
-__device__ __forceinline__ void prefetch_l2_bulk_hint(const void* ptr, uint32_t bytes, uint64_t pol) {
-    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes),
-                 "l"(pol)
-                 : "memory");
-}
-
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");

@@ -126,8 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                 const uint32_t bytes = diag ? kOperandBytes : kStageBytes;
                 int b = 0;
                 while (p.kb_start[b + 1] <= un.k0) ++b;
+                int pref = -1;  // batch whose successor's tensor map was prefetched
                 for (int kb = un.k0; kb < un.k1; ++kb) {
                     while (p.kb_start[b + 1] <= kb) ++b;
+                    if (b != pref) {
+                        // the next batch's map reaches the descriptor cache
+                        // while this batch's stages load
+                        if (b + 1 < p.n_batches) prefetch_tensormap(&p.maps[b + 1]);
+                        pref = b;
+                    }
                     const int tok = (kb - p.kb_start[b]) * kKBlock;
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, limit)) {
                         ok = false;

@@ -146,8 +146,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int xb = un.J * kTile + static_cast<int>(rank) * 64;
                 int b = 0;
                 while (p.kb_start[b + 1] <= un.k0) ++b;
+                int pref = -1;  // batch whose successor's tensor map was prefetched
                 for (int kb = un.k0; kb < un.k1; ++kb) {
                     while (p.kb_start[b + 1] <= kb) ++b;
+                    if (b != pref) {
+                        // the next batch's map reaches the descriptor cache
+                        // while this batch's stages load
+                        if (b + 1 < p.n_batches) prefetch_tensormap(&p.maps[b + 1]);
+                        pref = b;
+                    }
                     const int tok = (kb - p.kb_start[b]) * kKBlock;
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, limit)) {
                         ok = false;

@@ -109,8 +109,8 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
             // the tile's old values travel to L2 while the unit's MMAs run
             if (out_tile >= 0 && warp == first_warp && lane == 0) {
                 if (p.acc_mode == kAccLo)
-                    prefetch_l2_bulk_hint(p.acc + static_cast<size_t>(out_tile) * kTileWords + kTileElems,
-                                          kTileElems * sizeof(float), l2_policy_evict_last());
+                    prefetch_l2_bulk(p.acc + static_cast<size_t>(out_tile) * kTileWords + kTileElems,
+                                     kTileElems * sizeof(float));
                 else
                     prefetch_l2_bulk(p.acc + static_cast<size_t>(out_tile) * kTileWords,
                                      kTileWords * sizeof(float));
@@ -185,15 +185,12 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
             // in L2 by vector reductions (round to nearest, like an fp32
             // add): nothing comes back to the SM, so the epilogue moves on
             // to the next unit at once.
-            // The lo plane is kept in L2 ahead of other lines: the next small
-            // flush reads and adds to the same tiles.
-            const uint64_t pol = l2_policy_evict_last();
 #pragma unroll
             for (int q = 0; q < kEpiCols / 4; ++q) {
                 float4 v;
                 unpack2(add2(hi[2 * q], lo[2 * q]), v.x, v.y);
                 unpack2(add2(hi[2 * q + 1], lo[2 * q + 1]), v.z, v.w);
-                red_add_v4_f32_hint(out + kTileElems + q * 4 * kTile, v, pol);
+                red_add_v4_f32(out + kTileElems + q * 4 * kTile, v);
             }
           } else {
             // Sole writer of this tile in this launch: a plain read-modify-

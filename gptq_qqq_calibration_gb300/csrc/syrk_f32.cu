@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             Cursor L;
             cursor_start(p, L);
             uint32_t issued = 0;
+            int pref = -1;  // batch whose successor's tensor map was prefetched
             while (L.valid) {
+                if (L.b != pref) {
+                    if (L.b + 1 < p.n_batches) prefetch_tensormap(&p.maps[L.b + 1]);
+                    pref = L.b;
+                }
                 const int s = issued % kLand;
                 // a reused landing slot must have been read by every converter
                 if (issued >= static_cast<uint32_t>(kLand) &&
