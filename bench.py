@@ -40,10 +40,10 @@ F32_MMAS = 3  # tf32 MMAs per product in the fp32-input kernel
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with the SHA-256
 # of the kernel sources it was taken on.  When the sources differ the figure
 # no longer describes the kernel and the line reports traffic as null.
-SYRK_SOURCES = ["syrk_bf16.cu", "syrk_common.cuh", "ptx.cuh", "kernels.cuh"]
+SYRK_SOURCES = ["syrk_bf16.cu", "syrk_common.cuh", "schedule.cuh", "ptx.cuh", "kernels.cuh"]
 SYRK_DRAM_BYTES_PER_LAUNCH = {
     # workload: (bytes per launch, sources hash)
-    "d4096_ragged360_loguniform": (1.752e9, "30dcab472049ae53"),
+    "d4096_ragged360_loguniform": (1.753e9, "6d63d5ac87f34e53"),
 }
 
 

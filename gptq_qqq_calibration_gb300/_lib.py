@@ -14,9 +14,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgptq_hes
 
 HESS_BF16, HESS_F32 = 0, 1
 (HESS_OK, HESS_ERR_INVALID, HESS_ERR_UNSUPPORTED, HESS_ERR_OOM, HESS_ERR_CUDA, HESS_ERR_TIMEOUT,
- HESS_ERR_NOT_PD) = range(7)
+ HESS_ERR_NOT_PD, HESS_ERR_INTERNAL) = range(8)
 STATUS_NAMES = {0: "HESS_OK", 1: "HESS_ERR_INVALID", 2: "HESS_ERR_UNSUPPORTED", 3: "HESS_ERR_OOM",
-                4: "HESS_ERR_CUDA", 5: "HESS_ERR_TIMEOUT", 6: "HESS_ERR_NOT_PD"}
+                4: "HESS_ERR_CUDA", 5: "HESS_ERR_TIMEOUT", 6: "HESS_ERR_NOT_PD", 7: "HESS_ERR_INTERNAL"}
 OPTIONS = {"flush_tokens": 1, "max_pending": 2, "chunk_tokens": 3, "wait_timeout_ns": 4,
            "split_k": 5, "grid": 6, "pair_kernel": 7, "fold_every": 8,
            "overlap_launches": 9}

@@ -30,6 +30,7 @@
 // per bank) the drift is ~1e-6 of each update.  Every wait is bounded.
 #include <cuda.h>
 
+#include "device_ptr.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -406,6 +407,8 @@ EncodeTiledFn gemm_encode_fn() {
 cudaError_t encode_fp32(CUtensorMap* map, const float* ptr, int inner, int outer, int ld) {
     EncodeTiledFn fn = gemm_encode_fn();
     if (!fn) return cudaErrorNotSupported;
+    const cudaError_t ce = ensure_context();
+    if (ce != cudaSuccess) return ce;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
     const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(kKB)};

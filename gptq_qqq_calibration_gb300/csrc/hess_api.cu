@@ -20,6 +20,7 @@
 #include "device_ptr.h"
 #include "hess.h"
 #include "kernels.cuh"
+#include "schedule.cuh"
 
 #define HESS_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -70,6 +71,7 @@ hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, s
                       CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(HESS_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    CUDA_TRY(hk::ensure_context());
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem};
     cuuint32_t box[2] = {box_cols, box_rows};
@@ -129,7 +131,7 @@ struct hess_ctx {
     uint32_t* status_host = nullptr;
     cudaEvent_t ev_status = nullptr;
     bool status_copy_pending = false;
-    bool timed_out = false;  // a recorded device-side timeout was seen (until reset)
+    uint32_t fault = 0;  // a recorded device status word seen on the host (until reset)
     // The accumulator's last user: work on another stream waits for it
     // (flushes may read-modify-write tiles without atomics).
     cudaEvent_t ev_acc = nullptr;
@@ -312,14 +314,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
         p.acc_mode = next_acc_mode(h, p.exclusive);
-        // A single-slab flush whose last wave would fill at most half the
-        // grid runs that wave's tiles as two half units each (kAccLo adds
-        // them with reductions in L2, so two writers per tile are fine).
-        const int rem = p.n_tiles % grid_max;
-        p.tail_split = (p.exclusive && p.acc_mode == hk::kAccLo && p.n_tiles > grid_max && rem > 0 &&
-                        2 * rem <= grid_max && p.total_kb >= 2)
-                           ? rem
-                           : 0;
+        p.tail_split = hk::syrk::tail_split_for(p.n_tiles, grid_max, p.total_kb, p.exclusive != 0, p.acc_mode);
         p.n_units += p.tail_split;
         grid = std::min(grid_max, p.n_units);
         e = f32 ? hk::launch_syrk_f32(p, grid, stream, h->overlap != 0)
@@ -341,23 +336,31 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
     return HESS_OK;
 }
 
-// A device-side timeout recorded earlier and already visible on the host
-// (from the status copy of an earlier hess_materialize) fails the call.
+// The error a nonzero device status word stands for: an index guard that
+// failed (HESS_ERR_INTERNAL) before a wait that ran out (HESS_ERR_TIMEOUT).
+hess_status status_error(uint32_t st, const char* when) {
+    if (st & hk::kStatusBadIndex)
+        return fail(HESS_ERR_INTERNAL, "a kernel index guard failed%s (status 0x%x); hess_reset clears it", when, st);
+    return fail(HESS_ERR_TIMEOUT, "a device-side wait ran out%s (status 0x%x); hess_reset clears it", when, st);
+}
+
+// A device status recorded earlier and already visible on the host (from the
+// status copy of an earlier hess_materialize) fails the call.
 hess_status check_reported(hess_ctx* h) {
     if (h->status_copy_pending && cudaEventQuery(h->ev_status) == cudaSuccess) {
         h->status_copy_pending = false;
-        if (*reinterpret_cast<volatile uint32_t*>(h->status_host) != 0) h->timed_out = true;
+        h->fault |= *reinterpret_cast<volatile uint32_t*>(h->status_host);
     }
-    if (h->timed_out)
-        return fail(HESS_ERR_TIMEOUT, "a device-side wait of an earlier call ran out; hess_reset clears it");
+    if (h->fault) return status_error(h->fault, " in an earlier call");
     return HESS_OK;
 }
 
-hess_status read_status(uint32_t* dev_status, cudaStream_t stream) {
+hess_status read_status(uint32_t* dev_status, cudaStream_t stream, uint32_t* seen = nullptr) {
     uint32_t st = 0;
     CUDA_TRY(cudaMemcpyAsync(&st, dev_status, sizeof(st), cudaMemcpyDeviceToHost, stream));
     CUDA_TRY(cudaStreamSynchronize(stream));
-    if (st != 0) return fail(HESS_ERR_TIMEOUT, "a device-side wait ran out (status 0x%x)", st);
+    if (seen) *seen |= st;
+    if (st != 0) return status_error(st, "");
     return HESS_OK;
 }
 
@@ -492,11 +495,8 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
     if (damp_value_out) {
         float v = 0.0f;
         if (h->N != 0) CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
-        st = read_status(h->status, s);
-        if (st != HESS_OK) {
-            h->timed_out = true;
-            return st;
-        }
+        st = read_status(h->status, s, &h->fault);
+        if (st != HESS_OK) return st;
         *damp_value_out = v;
         return HESS_OK;
     }
@@ -527,9 +527,7 @@ HESS_EXPORT hess_status hess_sync(hess_t h, hess_stream_t stream) {
     std::lock_guard<std::mutex> lk(h->mu);
     hess_status st = check_device(h->device);
     if (st != HESS_OK) return st;
-    st = read_status(h->status, static_cast<cudaStream_t>(stream));
-    if (st == HESS_ERR_TIMEOUT) h->timed_out = true;
-    return st;
+    return read_status(h->status, static_cast<cudaStream_t>(stream), &h->fault);
 }
 
 HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
@@ -543,7 +541,7 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->pending_dtype = -1;
     h->N = 0;
     h->lo_flushes = 0;
-    h->timed_out = false;
+    h->fault = 0;
     h->status_copy_pending = false;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemsetAsync(h->acc, 0,
@@ -765,7 +763,7 @@ HESS_EXPORT hess_status hess_import_state(hess_t h, const void* src, int64_t byt
     h->pending.clear();
     h->pending_tokens = 0;
     h->pending_dtype = -1;
-    h->timed_out = false;
+    h->fault = 0;
     h->status_copy_pending = false;
     h->lo_flushes = std::min(static_cast<int>(tr[2]), h->fold_every - 1);
     if ((st = order_acc(h, s)) != HESS_OK) return st;

@@ -46,6 +46,9 @@ constexpr uint32_t kStatusTimeoutLoad = 1u;
 constexpr uint32_t kStatusTimeoutMma = 2u;
 constexpr uint32_t kStatusTimeoutEpilogue = 4u;
 constexpr uint32_t kStatusTimeoutDrain = 8u;
+// A kernel's index guard failed (a unit outside the upper triangle or the
+// flush, a batch or accumulator tile out of range): the access was skipped.
+constexpr uint32_t kStatusBadIndex = 16u;
 
 // How an exclusive (single-slab) launch adds a unit's compensated sum
 // (hi', lo') to its accumulator tile.  kAccPair renormalises the stored pair

@@ -149,6 +149,8 @@ extern "C" __attribute__((visibility("default"))) hess_status local_hess_compute
 
     EncodeTiledFn enc = noalloc_encode_fn();
     if (!enc) return noalloc_fail(HESS_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    err = hk::ensure_context();
+    if (err != cudaSuccess) return noalloc_fail(HESS_ERR_CUDA, "context: %s", cudaGetErrorString(err));
     hk::LocalParams p;
     std::memset(&p, 0, sizeof(p));
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_tokens)};

@@ -121,14 +121,14 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             uint32_t issued_par = 0;   // parity of the last load per stage
             for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
                 Unit un;
-                if (!unit_at(p, u, un)) continue;
+                if (!syrk::unit_checked(p, u, un)) continue;
                 const bool diag = un.I == un.J;
                 const uint32_t bytes = diag ? kOperandBytes : kStageBytes;
                 int b = 0;
-                while (p.kb_start[b + 1] <= un.k0) ++b;
+                while (b + 1 < p.n_batches && p.kb_start[b + 1] <= un.k0) ++b;
                 int pref = -1;  // batch whose successor's tensor map was prefetched
                 for (int kb = un.k0; kb < un.k1; ++kb) {
-                    while (p.kb_start[b + 1] <= kb) ++b;
+                    while (b + 1 < p.n_batches && p.kb_start[b + 1] <= kb) ++b;
                     if (b != pref) {
                         // the next batch's map reaches the descriptor cache
                         // while this batch's stages load
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             uint32_t aphase = 0;
             for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
                 Unit un;
-                if (!unit_at(p, u, un)) continue;
+                if (!syrk::unit_checked(p, u, un)) continue;
                 const bool diag = un.I == un.J;
                 for (int c0 = un.k0; c0 < un.k1; c0 += p.chunk_kb) {
                     const int c1 = min(c0 + p.chunk_kb, un.k1);

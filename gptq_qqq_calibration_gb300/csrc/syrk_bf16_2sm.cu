@@ -37,6 +37,7 @@ namespace {
 
 using syrk::kDrainLimitNs;
 using syrk::kEpiWarps;
+using syrk::PairUnit;
 
 constexpr int kStages = 4;
 constexpr uint32_t kBoxBytes = kKBlock * 128;       // kKBlock tokens x 64 bf16
@@ -58,26 +59,6 @@ constexpr uint32_t kIdesc = instr_desc_mn_major(1u /*bf16*/, 256, 128);
 constexpr int kNumBarriers = 2 * kStages + 5;
 constexpr unsigned long long kAbortSettleNs = 2000000ull;
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 8 * kNumBarriers + 16;
-
-struct PairUnit {
-    int I2, J, k0, k1;
-};
-
-__device__ __forceinline__ bool pair_unit_at(const SyrkParams& p, int u, PairUnit& un) {
-    const int slab = u / p.n_tiles;
-    const int t = u - slab * p.n_tiles;
-    const int T = p.tiles_per_dim;
-    int i = 0, rem = t;
-    while (rem >= T - 2 * i) {
-        rem -= T - 2 * i;
-        ++i;
-    }
-    un.I2 = i;
-    un.J = 2 * i + rem;
-    un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
-    un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
-    return un.k1 > un.k0;
-}
 
 template <bool kExcl>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -141,14 +122,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             for (int u = pair; ok && u < p.n_units; u += n_pairs) {
                 PairUnit un;
-                if (!pair_unit_at(p, u, un)) continue;
+                if (!syrk::pair_unit_checked(p, u, un)) continue;
                 const int xa = un.I2 * 256 + static_cast<int>(rank) * 128;
                 const int xb = un.J * kTile + static_cast<int>(rank) * 64;
                 int b = 0;
-                while (p.kb_start[b + 1] <= un.k0) ++b;
+                while (b + 1 < p.n_batches && p.kb_start[b + 1] <= un.k0) ++b;
                 int pref = -1;  // batch whose successor's tensor map was prefetched
                 for (int kb = un.k0; kb < un.k1; ++kb) {
-                    while (p.kb_start[b + 1] <= kb) ++b;
+                    while (b + 1 < p.n_batches && p.kb_start[b + 1] <= kb) ++b;
                     if (b != pref) {
                         // the next batch's map reaches the descriptor cache
                         // while this batch's stages load
@@ -188,7 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t aphase = 0;
             for (int u = pair; ok && u < p.n_units; u += n_pairs) {
                 PairUnit un;
-                if (!pair_unit_at(p, u, un)) continue;
+                if (!syrk::pair_unit_checked(p, u, un)) continue;
                 for (int c0 = un.k0; c0 < un.k1; c0 += p.chunk_kb) {
                     const int c1 = min(c0 + p.chunk_kb, un.k1);
                     if (!mbar_wait_cluster(acce_bar(ab), aphase ^ 1u, limit)) {
@@ -246,11 +227,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             p, tmem, warp, lane, kFirstEpiWarp, accf_bar(0), pair, n_pairs,
             [&](int u, int& k0, int& k1, int& out_tile) {
                 PairUnit un;
-                if (!pair_unit_at(p, u, un)) return false;
+                if (!syrk::pair_unit_checked(p, u, un)) return false;
                 k0 = un.k0;
                 k1 = un.k1;
-                const int rb = 2 * un.I2 + static_cast<int>(rank);
-                out_tile = (rb < T && rb <= un.J) ? tile_index(rb, un.J, T) : -1;
+                out_tile = syrk::pair_out_tile(un, static_cast<int>(rank), T);
                 return true;
             },
             [&](uint32_t bar, uint32_t parity) { return mbar_wait_cluster(bar, parity, limit); },

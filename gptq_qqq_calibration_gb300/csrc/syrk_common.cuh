@@ -4,60 +4,19 @@
 
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace hk {
 namespace syrk {
-
-// A unit is one 128x128 upper tile (I, J) over one slab [k0, k1) of the
-// flush's k-blocks.  Units are numbered slab-major so that the CTAs running
-// at the same time stream the same tokens.
-struct Unit {
-    int t, I, J, k0, k1;
-};
-
-// With p.tail_split > 0 (one slab): units below n_tiles - tail_split are
-// whole tiles; the rest are the last tail_split tiles, each as its first and
-// second half of the k-blocks.
-__device__ __forceinline__ bool unit_at(const SyrkParams& p, int u, Unit& un) {
-    int t;
-    if (p.tail_split > 0) {
-        const int whole = p.n_tiles - p.tail_split;
-        if (u < whole) {
-            t = u;
-            un.k0 = 0;
-            un.k1 = p.total_kb;
-        } else {
-            const int v = u - whole;
-            t = whole + (v >> 1);
-            const int mid = p.total_kb >> 1;
-            un.k0 = (v & 1) ? mid : 0;
-            un.k1 = (v & 1) ? p.total_kb : mid;
-        }
-    } else {
-        const int slab = u / p.n_tiles;
-        t = u - slab * p.n_tiles;
-        un.k0 = static_cast<int>(static_cast<long long>(slab) * p.total_kb / p.n_slabs);
-        un.k1 = static_cast<int>(static_cast<long long>(slab + 1) * p.total_kb / p.n_slabs);
-    }
-    int i = 0, rem = t;
-    while (rem >= p.tiles_per_dim - i) {
-        rem -= p.tiles_per_dim - i;
-        ++i;
-    }
-    un.t = t;
-    un.I = i;
-    un.J = i + rem;
-    return un.k1 > un.k0;
-}
 
 // Before the wait for the previous grid (which reads nothing of the
 // previous kernel's output): the first unit's tensor map is fetched into
 // the descriptor cache and the parameters into the constant cache.
 __device__ __forceinline__ void prefetch_first_map(const SyrkParams& p) {
     Unit un;
-    if (static_cast<int>(blockIdx.x) < p.n_units && unit_at(p, blockIdx.x, un)) {
+    if (static_cast<int>(blockIdx.x) < p.n_units && unit_at(p, blockIdx.x, un) && unit_in_range(p, un)) {
         int b = 0;
-        while (p.kb_start[b + 1] <= un.k0) ++b;
+        while (b + 1 < p.n_batches && p.kb_start[b + 1] <= un.k0) ++b;
         prefetch_tensormap(&p.maps[b]);
     }
 }
@@ -176,6 +135,10 @@ __device__ __forceinline__ void epilogue_t(const SyrkParams& p, uint32_t tmem, i
         }
         if (!ok) break;
         if (out_tile < 0) continue;
+        if (out_tile >= p.tiles_per_dim * (p.tiles_per_dim + 1) / 2) {  // guard: not a tile of H
+            atomicOr(p.status, kStatusBadIndex);
+            continue;
+        }
         // this thread's row of the hi plane, from column col0 on (4-column
         // blocks of 4 words); the lo plane is kTileElems further
         float* const out = p.acc + static_cast<size_t>(out_tile) * kTileWords + tile_offset(row, col0);
@@ -303,7 +266,7 @@ __device__ __forceinline__ void epilogue(const SyrkParams& p, uint32_t tmem, int
         p, tmem, warp, lane, first_warp, accf_bar0, blockIdx.x, gridDim.x,
         [&](int u, int& k0, int& k1, int& out_tile) {
             Unit un;
-            if (!unit_at(p, u, un)) return false;
+            if (!unit_checked(p, u, un)) return false;
             k0 = un.k0;
             k1 = un.k1;
             out_tile = un.t;

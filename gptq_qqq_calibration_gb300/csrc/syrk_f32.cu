@@ -78,10 +78,10 @@ struct Cursor {
 
 __device__ __forceinline__ void cursor_seek(const SyrkParams& p, Cursor& c) {
     while (c.u < p.n_units) {
-        if (unit_at(p, c.u, c.un)) {
+        if (syrk::unit_checked(p, c.u, c.un)) {
             c.kb = c.un.k0;
             c.b = 0;
-            while (p.kb_start[c.b + 1] <= c.kb) ++c.b;
+            while (c.b + 1 < p.n_batches && p.kb_start[c.b + 1] <= c.kb) ++c.b;
             c.valid = true;
             return;
         }
@@ -97,7 +97,7 @@ __device__ __forceinline__ void cursor_start(const SyrkParams& p, Cursor& c) {
 
 __device__ __forceinline__ void cursor_next(const SyrkParams& p, Cursor& c) {
     if (++c.kb < c.un.k1) {
-        while (p.kb_start[c.b + 1] <= c.kb) ++c.b;
+        while (c.b + 1 < p.n_batches && p.kb_start[c.b + 1] <= c.kb) ++c.b;
         return;
     }
     c.u += gridDim.x;
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_f32_kernel(const __grid_cons
             uint32_t aphase = 0;
             for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
                 Unit un;
-                if (!unit_at(p, u, un)) continue;
+                if (!syrk::unit_checked(p, u, un)) continue;
                 const bool diag = un.I == un.J;
                 for (int c0 = un.k0; c0 < un.k1; c0 += p.chunk_kb) {
                     const int c1 = min(c0 + p.chunk_kb, un.k1);

@@ -69,7 +69,10 @@ typedef enum {
     HESS_ERR_OOM = 3,         /* device or host allocation failed (create only) */
     HESS_ERR_CUDA = 4,        /* a CUDA call failed; see hess_last_error() */
     HESS_ERR_TIMEOUT = 5,     /* a device-side wait ran out; results are invalid */
-    HESS_ERR_NOT_PD = 6       /* gptq_prepare: the damped Hessian has no fp32 Cholesky factor */
+    HESS_ERR_NOT_PD = 6,      /* gptq_prepare: the damped Hessian has no fp32 Cholesky factor */
+    HESS_ERR_INTERNAL = 7     /* a kernel's index guard failed (a library defect): the access
+                                 was skipped and the results are invalid; reported like a
+                                 timeout (hess_sync, or the calls that report a timeout) */
 } hess_status;
 
 /* Options for hess_set_option. */

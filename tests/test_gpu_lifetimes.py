@@ -28,36 +28,51 @@ def _built():
 def test_clone_while_another_thread_adds():
     """A clone holds exactly the batches its token count counts: the flush,
     the copy of the sums and the read of N happen under one hold of the
-    source's lock, while a second thread keeps adding batches on its own
-    stream.  Every clone must equal the oracle over the prefix of batches
-    that its N names."""
-    from gptq_qqq_calibration_gb300 import Hessian
+    source's mutex, while a second host thread keeps adding batches on its
+    own stream.  Both threads call the C ABI directly (ctypes releases the
+    interpreter lock), so the handle's mutex is the only thing ordering
+    them.  Every clone must equal the oracle over the prefix of batches that
+    its N names."""
+    import ctypes
+
+    from gptq_qqq_calibration_gb300 import _lib, hess_create, hess_destroy
+    L = _lib.load()
     d = 256
     counts = np.random.default_rng(31).integers(1, 200, size=800)
     xs = list(batches(d, counts, seed=31))
     torch.cuda.synchronize()
-    src = Hessian(d, flush_tokens=3000)
-    clones = []
-    # Clone j runs while the adder adds batches 50 j .. 50 j + 49; the adder
-    # then waits for it, so the clones land at different points of the stream.
+    src = hess_create(d)
+    assert L.hess_set_option(src, _lib.OPTIONS["flush_tokens"], 3000) == _lib.HESS_OK
+    s_add, s_clone = torch.cuda.Stream(), torch.cuda.Stream()
+    clones, errors = [], []
+    # Clone j starts once the adder has begun batch 50 j and runs while it
+    # adds batches 50 j .. 50 j + 49; the adder then waits for it, so every
+    # clone lands at a different point of the stream, in the middle of adds.
     n_clones = 15
+    reached = [threading.Event() for _ in range(n_clones)]
     done = [threading.Event() for _ in range(n_clones)]
 
     def adder():
-        s = torch.cuda.Stream()
-        with torch.cuda.stream(s):
-            for k, X in enumerate(xs):
-                src.add_batch(X, stream=s)
-                j = k // 50
-                if k % 50 == 49 and j < n_clones:
-                    done[j].wait(60)
+        for k, X in enumerate(xs):
+            j = k // 50
+            if k % 50 == 0 and j < n_clones:
+                reached[j].set()
+            st = L.hess_add_batch(src, X.data_ptr(), X.shape[0], 0, s_add.cuda_stream)
+            if st != _lib.HESS_OK:
+                errors.append(("add", st, L.hess_last_error()))
+            if k % 50 == 49 and j < n_clones:
+                done[j].wait(60)
 
     def cloner():
-        s = torch.cuda.Stream()
-        with torch.cuda.stream(s):
-            for j in range(n_clones):
-                clones.append(src.clone(stream=s))
-                done[j].set()
+        for j in range(n_clones):
+            reached[j].wait(60)
+            out = ctypes.c_void_p()
+            st = L.hess_clone(src, ctypes.byref(out), s_clone.cuda_stream)
+            if st != _lib.HESS_OK:
+                errors.append(("clone", st, L.hess_last_error()))
+            else:
+                clones.append(out.value)
+            done[j].set()
 
     ta, tc = threading.Thread(target=adder), threading.Thread(target=cloner)
     ta.start()
@@ -65,31 +80,34 @@ def test_clone_while_another_thread_adds():
     ta.join(120)
     tc.join(120)
     assert not ta.is_alive() and not tc.is_alive()
+    assert not errors, errors
     torch.cuda.synchronize()
     prefix = np.concatenate([[0], np.cumsum(counts)])
-    assert src.n_tokens == prefix[-1]
+    assert L.hess_token_count(src) == prefix[-1]
     want = {}
     for c in clones:
-        k = int(np.searchsorted(prefix, c.n_tokens))
-        assert prefix[k] == c.n_tokens, "a clone's N must end on a batch boundary"
+        n = L.hess_token_count(c)
+        k = int(np.searchsorted(prefix, n))
+        assert prefix[k] == n, "a clone's N must end on a batch boundary"
         want.setdefault(k, []).append(c)
     assert len(want) >= 4, f"the clones should see several prefixes of the stream: {sorted(want)}"
     o = GramOracle(d)
-    done = 0
+    done_k = 0
+    H = torch.empty((d, d), dtype=torch.float32, device="cuda")
     for k in sorted(want):
-        for X in xs[done:k]:
+        for X in xs[done_k:k]:
             o.add_batch(host(X))
-        done = k
+        done_k = k
         Href = o.hessian()
         for c in want[k]:
-            H, _ = c.materialize(0.0)
-            c.sync()
+            assert L.hess_materialize(c, H.data_ptr(), 0.0, None, None) == _lib.HESS_OK
+            assert L.hess_sync(c, None) == _lib.HESS_OK
             if k == 0:
                 assert not torch.any(H)
             else:
                 assert rel_err(H.cpu().numpy(), Href) <= TOL_BF16, f"clone at {k} batches"
-            c.close()
-    src.close()
+            hess_destroy(c)
+    hess_destroy(src)
 
 
 def test_flushed_batch_is_not_reused_before_its_side_stream_flush_runs():
@@ -152,3 +170,34 @@ def test_timeout_reaches_a_caller_that_does_not_wait():
     h.sync()
     assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
     h.close()
+
+
+def test_first_call_on_a_new_host_thread_flushes():
+    """A host thread whose first CUDA call is the library's: an add_batch
+    that flushes at once (one batch, one stream, so nothing else binds a
+    context before the tensor map is encoded).  The library binds the
+    device's primary context for its driver calls; the call succeeds and
+    the sum is the oracle's."""
+    from gptq_qqq_calibration_gb300 import _lib, hess_create, hess_destroy
+    L = _lib.load()
+    d = 384
+    X = next(batches(d, [700], seed=35))
+    torch.cuda.synchronize()
+    h = hess_create(d)
+    assert L.hess_set_option(h, _lib.OPTIONS["flush_tokens"], 1) == _lib.HESS_OK
+    res = []
+
+    def worker():
+        res.append((L.hess_add_batch(h, X.data_ptr(), X.shape[0], 0, None), L.hess_last_error()))
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join(60)
+    assert res and res[0][0] == _lib.HESS_OK, res
+    H = torch.empty((d, d), dtype=torch.float32, device="cuda")
+    assert L.hess_materialize(h, H.data_ptr(), 0.0, None, None) == _lib.HESS_OK
+    assert L.hess_sync(h, None) == _lib.HESS_OK
+    o = GramOracle(d)
+    o.add_batch(host(X))
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    hess_destroy(h)
