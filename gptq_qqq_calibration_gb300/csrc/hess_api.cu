@@ -111,6 +111,10 @@ bool injected_alloc_failure() {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The handle's device status block: word 0 the status bits the kernels OR
+// in, words 8..11 the state-blob trailer staged for a copy.
+constexpr size_t kStatusBytes = 64;
+
 }  // namespace
 
 struct hess_ctx {
@@ -125,10 +129,12 @@ struct hess_ctx {
     double* damp64 = nullptr;  // the damping value, then materialize's scratch
     float* damp32 = nullptr;
     cudaEvent_t ev = nullptr;
-    // Pinned host copy of the status word, refreshed by an asynchronous copy
-    // that every hess_materialize enqueues; the next call on the handle reads
-    // it once ev_status has completed, without waiting.
+    // Pinned, mapped host copy of the status word (word 0) and of the damping
+    // value (word 1), written by the materialize kernel itself (or by a copy
+    // when N == 0).  The next call on the handle reads it once ev_status has
+    // completed, without waiting.
     uint32_t* status_host = nullptr;
+    uint32_t* status_host_dev = nullptr;  // its device address
     cudaEvent_t ev_status = nullptr;
     bool status_copy_pending = false;
     uint32_t fault = 0;  // a recorded device status word seen on the host (until reset)
@@ -393,24 +399,25 @@ HESS_EXPORT hess_status hess_create(int64_t d, hess_t* out) {
     h->T = static_cast<int>(ceil_div(d, hk::kTile));
     h->n_tiles = h->T * (h->T + 1) / 2;
     cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    // The status block sits right after the accumulator tiles, so that one
+    // memset clears both in hess_reset.
     const size_t acc_bytes = static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float);
-    if (e == cudaSuccess) e = cudaMalloc(&h->acc, acc_bytes);
-    if (e == cudaSuccess) e = cudaMalloc(&h->status, 64);
+    if (e == cudaSuccess) e = cudaMalloc(&h->acc, acc_bytes + kStatusBytes);
+    if (e == cudaSuccess) h->status = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(h->acc) + acc_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&h->damp64, hk::materialize_scratch_bytes(h->T));
     if (e == cudaSuccess) e = cudaMalloc(&h->damp32, sizeof(float));
-    if (e == cudaSuccess) e = cudaMemset(h->acc, 0, acc_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->acc, 0, acc_bytes + kStatusBytes);
     if (e == cudaSuccess) e = cudaMemset(h->damp64, 0, hk::materialize_scratch_bytes(h->T));
-    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 64);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_acc, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_status, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaHostAlloc(&h->status_host, 64, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaHostAlloc(&h->status_host, 64, cudaHostAllocMapped);
     if (e == cudaSuccess) std::memset(h->status_host, 0, 64);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->status_host_dev), h->status_host, 0);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         hess_status s = e == cudaErrorMemoryAllocation ? HESS_ERR_OOM : HESS_ERR_CUDA;
         cudaFree(h->acc);
-        cudaFree(h->status);
         cudaFree(h->damp64);
         cudaFree(h->damp32);
         if (h->status_host) cudaFreeHost(h->status_host);
@@ -485,25 +492,35 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
     if (st != HESS_OK) return st;
     if (h->N == 0) {
         CUDA_TRY(cudaMemsetAsync(H_out, 0, static_cast<size_t>(h->d) * h->d * sizeof(float), s));
+        if (damp_value_out) {
+            *damp_value_out = 0.0f;
+            return read_status(h->status, s, &h->fault);
+        }
+        // the status word travels to the pinned host copy behind this work
+        CUDA_TRY(cudaMemcpyAsync(h->status_host, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
     } else {
         const double scale = 2.0 / static_cast<double>(h->N);
         if ((st = order_acc(h, s)) != HESS_OK) return st;
         CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, damp_percent,
-                                        h->damp64, h->damp32, s));
+                                        h->damp64, h->damp32, h->status, h->status_host_dev, s));
         if ((st = mark_acc(h, s)) != HESS_OK) return st;
     }
+    CUDA_TRY(cudaEventRecord(h->ev_status, s));
     if (damp_value_out) {
-        float v = 0.0f;
-        if (h->N != 0) CUDA_TRY(cudaMemcpyAsync(&v, h->damp32, sizeof(float), cudaMemcpyDeviceToHost, s));
-        st = read_status(h->status, s, &h->fault);
-        if (st != HESS_OK) return st;
+        // the kernel wrote the status word and the damping value to the
+        // pinned host copy: wait for it, then read both there
+        CUDA_TRY(cudaEventSynchronize(h->ev_status));
+        h->status_copy_pending = false;
+        const volatile uint32_t* m = h->status_host;
+        h->fault |= m[0];
+        if (m[0] != 0) return status_error(m[0], "");
+        uint32_t bits = m[1];
+        float v;
+        std::memcpy(&v, &bits, sizeof(v));
         *damp_value_out = v;
         return HESS_OK;
     }
-    // No wait here: the status word travels to the pinned host copy behind
-    // this call's work, and a later call reports a timeout it shows.
-    CUDA_TRY(cudaMemcpyAsync(h->status_host, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaEventRecord(h->ev_status, s));
+    // No wait here: a later call reports a timeout the host copy shows.
     h->status_copy_pending = true;
     return HESS_OK;
 }
@@ -544,9 +561,9 @@ HESS_EXPORT hess_status hess_reset(hess_t h, hess_stream_t stream) {
     h->fault = 0;
     h->status_copy_pending = false;
     if ((st = order_acc(h, s)) != HESS_OK) return st;
+    // the tiles and the status block after them, in one memset
     CUDA_TRY(cudaMemsetAsync(h->acc, 0,
-                             static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float), s));
-    CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
+                             static_cast<size_t>(h->n_tiles) * hk::kTileWords * sizeof(float) + kStatusBytes, s));
     return mark_acc(h, s);
 }
 
@@ -608,7 +625,6 @@ HESS_EXPORT hess_status hess_destroy(hess_t h) {
         cudaSetDevice(h->device);
         cudaDeviceSynchronize();
         cudaFree(h->acc);
-        cudaFree(h->status);
         cudaFree(h->damp64);
         cudaFree(h->damp32);
         cudaFreeHost(h->status_host);
@@ -768,7 +784,7 @@ HESS_EXPORT hess_status hess_import_state(hess_t h, const void* src, int64_t byt
     h->lo_flushes = std::min(static_cast<int>(tr[2]), h->fold_every - 1);
     if ((st = order_acc(h, s)) != HESS_OK) return st;
     CUDA_TRY(cudaMemcpyAsync(h->acc, src, ab, cudaMemcpyDefault, s));
-    CUDA_TRY(cudaMemsetAsync(h->status, 0, 64, s));
+    CUDA_TRY(cudaMemsetAsync(h->status, 0, kStatusBytes, s));
     h->N = n_tokens;
     return mark_acc(h, s);
 }

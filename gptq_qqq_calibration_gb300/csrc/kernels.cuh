@@ -139,8 +139,13 @@ cudaError_t launch_syrk_f32(const SyrkParams& p, int grid, cudaStream_t s, bool 
 // Scratch of one materialization: the fp64 damping value, per-quarter sums
 // of the diagonal and an arrival count (zeroed once, left zero by each launch).
 size_t materialize_scratch_bytes(int T);
+// The kernel waits for the previous kernel of the stream (it is launched to
+// overlap that kernel's end).  With status_mirror non-null (a device pointer
+// to mapped pinned host memory) it also writes there *status (word 0) and
+// the fp32 damping value (word 1).
 cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
-                               double damp_percent, double* scratch, float* damp_f32, cudaStream_t s);
+                               double damp_percent, double* scratch, float* damp_f32, const uint32_t* status,
+                               uint32_t* status_mirror, cudaStream_t s);
 
 // Local 16x16 block Grams.
 constexpr int kLocalKBlock = 64;   // tokens per stage

@@ -43,8 +43,13 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
                                                           double scale, float scale_hi,
                                                           float scale_lo, double damp_percent,
                                                           double* __restrict__ scratch,
-                                                          float* __restrict__ damp_f32) {
+                                                          float* __restrict__ damp_f32,
+                                                          const uint32_t* __restrict__ status,
+                                                          uint32_t* __restrict__ status_mirror) {
     __shared__ float tr[64][65];
+    // Launched to overlap the end of the flush before it: the accumulator
+    // is read only once that kernel has completed.
+    griddep_wait();
     __shared__ double wpart[8];
     __shared__ int last;
     const int a = (blockIdx.x >> 1) & 1, b = blockIdx.x & 1;
@@ -141,6 +146,15 @@ __global__ void __launch_bounds__(256) materialize_kernel(const float* __restric
         scratch[0] = damp;
         *damp_f32 = static_cast<float>(damp);
         *ticket = 0u;  // ready for the next launch (every quarter has arrived)
+        // the handle's status word and the damping value, written straight
+        // to their pinned host copy (mapped memory): the host reads them
+        // there once this kernel has completed, with no copy in the stream
+        if (status_mirror != nullptr) {
+            volatile uint32_t* m = status_mirror;
+            m[0] = *status;
+            m[1] = __float_as_uint(static_cast<float>(damp));
+            __threadfence_system();
+        }
         wpart[0] = damp;
     }
     __syncthreads();
@@ -167,13 +181,22 @@ __global__ void __launch_bounds__(256) local_read_kernel(const double* __restric
 size_t materialize_scratch_bytes(int T) { return ticket_offset(T) + sizeof(unsigned); }
 
 cudaError_t launch_materialize(const float* acc, float* H_out, int d, int T, double scale,
-                               double damp_percent, double* scratch, float* damp_f32, cudaStream_t s) {
+                               double damp_percent, double* scratch, float* damp_f32, const uint32_t* status,
+                               uint32_t* status_mirror, cudaStream_t s) {
     const int n_tiles = T * (T + 1) / 2;
     const float scale_hi = static_cast<float>(scale);
     const float scale_lo = static_cast<float>(scale - static_cast<double>(scale_hi));
-    materialize_kernel<<<4 * n_tiles, 256, 0, s>>>(acc, H_out, d, T, scale, scale_hi, scale_lo,
-                                                        damp_percent, scratch, damp_f32);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(4 * n_tiles), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, materialize_kernel, acc, H_out, d, T, scale, scale_hi, scale_lo, damp_percent,
+                              scratch, damp_f32, status, status_mirror);
 }
 
 cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, double scale,
