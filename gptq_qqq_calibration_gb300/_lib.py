@@ -32,6 +32,7 @@ PROTOTYPES = {
     "hess_materialize": (_i32, [_vp, _vp, _f64, _vp, _fp]),
     "hess_token_count": (_i64, [_vp]),
     "hess_pending_batches": (_i64, [_vp]),
+    "hess_kernel_launches": (_i64, [_vp]),
     "hess_dim": (_i64, [_vp]),
     "hess_sync": (_i32, [_vp, _vp]),
     "hess_reset": (_i32, [_vp, _vp]),

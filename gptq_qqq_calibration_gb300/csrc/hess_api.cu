@@ -144,6 +144,7 @@ struct hess_ctx {
     cudaStream_t acc_stream = nullptr;
     bool acc_used = false;
     int64_t N = 0;
+    int64_t kernels = 0;  // kernel launches made for this handle (hess_kernel_launches)
     struct Pending {
         const void* ptr;
         int64_t n;
@@ -313,10 +314,24 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         p.tail_split = 0;
         grid = 2 * std::min(pairs_max, p.n_units);
         e = hk::launch_syrk_bf16_2sm(p, grid, stream, h->overlap != 0);
+        ++h->kernels;
     } else {
         const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(h->n_tiles, p.total_kb, kblock, grid_max);
+        if (h->split_k == 0 && p.n_slabs > 1 && h->fold_every > 1) {
+            // A large flush runs as one slab that adds to the low part with
+            // L2 reductions, its last wave split in halves (tail_split_for):
+            // the waves stay balanced without split-K's compensated atomics
+            // on both parts.  A fold that is due goes first, as its own
+            // pass over the accumulator.
+            if (h->lo_flushes + 1 >= h->fold_every) {
+                CUDA_TRY(hk::launch_renorm_pairs(h->acc, static_cast<size_t>(h->n_tiles), h->sm_count, stream));
+                ++h->kernels;
+                h->lo_flushes = 0;
+            }
+            p.n_slabs = 1;
+        }
         p.n_units = p.n_tiles * p.n_slabs;
         p.exclusive = p.n_slabs == 1 ? 1 : 0;
         p.acc_mode = next_acc_mode(h, p.exclusive);
@@ -325,6 +340,7 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         grid = std::min(grid_max, p.n_units);
         e = f32 ? hk::launch_syrk_f32(p, grid, stream, h->overlap != 0)
                 : hk::launch_syrk_bf16(p, grid, stream, h->overlap != 0);
+        ++h->kernels;
     }
     h->pending.clear();
     h->pending_tokens = 0;
@@ -503,6 +519,7 @@ HESS_EXPORT hess_status hess_materialize(hess_t h, float* H_out, double damp_per
         if ((st = order_acc(h, s)) != HESS_OK) return st;
         CUDA_TRY(hk::launch_materialize(h->acc, H_out, static_cast<int>(h->d), h->T, scale, damp_percent,
                                         h->damp64, h->damp32, h->status, h->status_host_dev, s));
+        ++h->kernels;
         if ((st = mark_acc(h, s)) != HESS_OK) return st;
     }
     CUDA_TRY(cudaEventRecord(h->ev_status, s));
@@ -529,6 +546,12 @@ HESS_EXPORT int64_t hess_token_count(hess_t h) {
     if (!h) return -1;
     std::lock_guard<std::mutex> lk(h->mu);
     return h->N;
+}
+
+HESS_EXPORT int64_t hess_kernel_launches(hess_t h) {
+    if (!h) return -1;
+    std::lock_guard<std::mutex> lk(h->mu);
+    return h->kernels;
 }
 
 HESS_EXPORT int64_t hess_pending_batches(hess_t h) {
@@ -659,6 +682,7 @@ HESS_EXPORT hess_status hess_merge(hess_t dst, hess_t src, hess_stream_t stream)
     if ((st = flush_locked(dst, s)) != HESS_OK) return st;
     if ((st = order_acc(src, s)) != HESS_OK || (st = order_acc(dst, s)) != HESS_OK) return st;
     CUDA_TRY(hk::launch_add_pairs(dst->acc, src->acc, static_cast<size_t>(dst->n_tiles), dst->sm_count, s));
+    ++dst->kernels;
     if ((st = mark_acc(src, s)) != HESS_OK || (st = mark_acc(dst, s)) != HESS_OK) return st;
     dst->N += src->N;
     dst->lo_flushes = 0;  // the merge leaves dst's pairs renormalised

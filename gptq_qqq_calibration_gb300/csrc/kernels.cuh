@@ -170,6 +170,9 @@ cudaError_t launch_local_read(const double* acc, float* out, int n_blocks, doubl
 cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                cudaStream_t s);
 
+// (hi, lo) <- TwoSum(hi, lo) over n_tiles accumulator tiles (folds lo into hi).
+cudaError_t launch_renorm_pairs(float* acc, size_t n_tiles, int sm_count, cudaStream_t s);
+
 // dst += src over n_tiles (hi, lo) accumulator tiles (accumulator merge).
 cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int sm_count,
                              cudaStream_t s);

@@ -149,7 +149,36 @@ cudaError_t launch_add_pairs(float* dst, const float* src, size_t n_tiles, int s
 
 namespace {
 __global__ void store_words_kernel(uint4* dst, uint4 v) { *dst = v; }
+
+// (hi, lo) <- TwoSum(hi, lo) over accumulator tiles: folds the low part's
+// undigested flush sums into the high part, exactly.  Four elements per
+// thread, grid-stride over the tiles' planes.
+__global__ void __launch_bounds__(256) renorm_pairs_kernel(float* __restrict__ acc, size_t n_tiles) {
+    const size_t per_tile = kTileElems / 4;
+    const size_t n4 = n_tiles * per_tile;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t q = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; q < n4; q += stride) {
+        const size_t t = q / per_tile, k = (q - t * per_tile) * 4;
+        float* h = acc + t * kTileWords + k;
+        float4 a = *reinterpret_cast<const float4*>(h);
+        float4 b = *reinterpret_cast<const float4*>(h + kTileElems);
+        float e;
+        a.x = two_sum(a.x, b.x, e); b.x = e;
+        a.y = two_sum(a.y, b.y, e); b.y = e;
+        a.z = two_sum(a.z, b.z, e); b.z = e;
+        a.w = two_sum(a.w, b.w, e); b.w = e;
+        *reinterpret_cast<float4*>(h) = a;
+        *reinterpret_cast<float4*>(h + kTileElems) = b;
+    }
+}
 }  // namespace
+
+cudaError_t launch_renorm_pairs(float* acc, size_t n_tiles, int sm_count, cudaStream_t s) {
+    const size_t want = (n_tiles * (kTileElems / 4) + 255) / 256;
+    const int grid = static_cast<int>(want < static_cast<size_t>(4 * sm_count) ? want : 4 * sm_count);
+    renorm_pairs_kernel<<<grid, 256, 0, s>>>(acc, n_tiles);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                cudaStream_t s) {

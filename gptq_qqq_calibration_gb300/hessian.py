@@ -23,7 +23,8 @@ from ._lib import HESS_BF16, HESS_F32, HessError, check
 __all__ = [
     "HESS_BF16", "HESS_F32", "HessError",
     "hess_create", "hess_add_batch", "hess_flush", "hess_materialize", "hess_token_count",
-    "hess_pending_batches", "hess_sync", "hess_reset", "hess_set_option", "hess_destroy",
+    "hess_pending_batches", "hess_kernel_launches", "hess_sync", "hess_reset", "hess_set_option",
+    "hess_destroy",
     "local_hess_create", "local_hess_add", "local_hess_read", "local_hess_token_count",
     "local_hess_sync", "local_hess_reset", "local_hess_destroy",
     "hess_merge", "hess_clone", "hess_state_bytes", "hess_export_state", "hess_import_state",
@@ -88,6 +89,10 @@ def hess_token_count(h: int) -> int:
 
 def hess_pending_batches(h: int) -> int:
     return int(_lib.load().hess_pending_batches(h))
+
+
+def hess_kernel_launches(h: int) -> int:
+    return int(_lib.load().hess_kernel_launches(h))
 
 
 def hess_sync(h: int, stream=None) -> None:

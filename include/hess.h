@@ -94,12 +94,14 @@ typedef enum {
     HESS_OPT_PAIR_KERNEL = 7,     /* bf16: 0 = tiles of 128x128, one SM each (default),
                                      1 = tiles of 256x128 on pairs of SMs (fewer operand
                                      bytes per SM; faster with long chunks) */
-    HESS_OPT_FOLD_EVERY = 8,      /* 1..64, default 8: of this many single-slab flushes, one
-                                     updates both fp32 parts of the accumulator and the others
-                                     only its low part, which halves the accumulator bytes a
-                                     small flush moves; the low part holds at most this many
-                                     minus one flushes' sums between folds.  1 = every flush
-                                     updates both parts. */
+    HESS_OPT_FOLD_EVERY = 8,      /* 1..64, default 8: the accumulator keeps each entry as two
+                                     fp32 parts; most flushes add only to the low part (half
+                                     the accumulator bytes of a small flush, and large flushes
+                                     run as one balanced slab), and at most this many minus one
+                                     flushes' sums wait in the low part before they are folded
+                                     into the high part (by the next small flush, or by a pass of
+                                     its own before a large one).  1 = every flush updates both
+                                     parts exactly (large flushes then use split-K). */
     HESS_OPT_OVERLAP_LAUNCHES = 9 /* 1 (default): a flush's kernel is launched so that it may
                                      be scheduled while the kernel before it in the stream
                                      ends (programmatic dependent launch); it sets itself up
@@ -181,6 +183,10 @@ hess_status hess_materialize(hess_t h, float* H_out, double damp_percent, hess_s
 int64_t hess_token_count(hess_t h);
 /* Number of the most recently added batches that are still queued. */
 int64_t hess_pending_batches(hess_t h);
+/* Kernels this handle has launched so far (flush passes, fold passes,
+ * materializations, merges into it), or -1 for NULL.  A diagnostic count; it
+ * is not reset by hess_reset. */
+int64_t hess_kernel_launches(hess_t h);
 /* Width d of the handle, or -1 for NULL. */
 int64_t hess_dim(hess_t h);
 

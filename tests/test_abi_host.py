@@ -97,6 +97,7 @@ def test_more_entry_points_reject_bad_arguments_before_cuda(lib):
     assert lib.hess_export_state(None, None, 0, None, ctypes.byref(n)) == HESS_ERR_INVALID
     assert lib.hess_import_state(None, None, 0, 0, None) == HESS_ERR_INVALID
     assert lib.hess_pending_batches(None) == -1
+    assert lib.hess_kernel_launches(None) == -1
     assert lib.hess_dim(None) == -1
     assert lib.hess_sync(None, None) == HESS_ERR_INVALID
     assert lib.hess_reset(None, None) == HESS_ERR_INVALID
