@@ -319,12 +319,14 @@ hess_status flush_locked(hess_ctx* h, cudaStream_t stream) {
         const int grid_max = h->grid > 0 ? h->grid : h->sm_count;
         p.n_slabs = h->split_k > 0 ? std::min(h->split_k, p.total_kb)
                                    : choose_slabs(h->n_tiles, p.total_kb, kblock, grid_max);
-        if (h->split_k == 0 && p.n_slabs > 1 && h->fold_every > 1) {
-            // A large flush runs as one slab that adds to the low part with
-            // L2 reductions, its last wave split in halves (tail_split_for):
-            // the waves stay balanced without split-K's compensated atomics
-            // on both parts.  A fold that is due goes first, as its own
-            // pass over the accumulator.
+        if (!f32 && h->split_k == 0 && p.n_slabs > 1 && h->fold_every > 1) {
+            // A large bf16 flush runs as one slab that adds to the low part
+            // with L2 reductions, its last wave split in halves
+            // (tail_split_for): the waves stay balanced without split-K's
+            // compensated atomics on both parts.  A fold that is due goes
+            // first, as its own pass over the accumulator.  (The fp32
+            // kernel, bound by its converters, measured 2 % faster with
+            // split-K, and keeps it.)
             if (h->lo_flushes + 1 >= h->fold_every) {
                 CUDA_TRY(hk::launch_renorm_pairs(h->acc, static_cast<size_t>(h->n_tiles), h->sm_count, stream));
                 ++h->kernels;
