@@ -45,6 +45,15 @@ hess_status fail(hess_status s, const char* fmt, ...) {
             return fail(HESS_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
     } while (0)
 
+// Host-side fault injection for tests: HESS_FAULT=alloc makes the *_create
+// calls fail as if out of memory; HESS_FAULT=encode makes every tensor-map
+// encoding fail as if the driver refused the descriptor.
+bool injected(const char* what) {
+    const char* f = std::getenv("HESS_FAULT");
+    return f && std::strcmp(f, what) == 0;
+}
+bool injected_alloc_failure() { return injected("alloc"); }
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -71,6 +80,7 @@ hess_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dt, s
                       CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(HESS_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    if (injected("encode")) return fail(HESS_ERR_UNSUPPORTED, "injected tensor-map failure (HESS_FAULT=encode)");
     CUDA_TRY(hk::ensure_context());
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem};
@@ -104,10 +114,6 @@ hess_status prepare_device(int dev, int* max_pairs) {
     return HESS_OK;
 }
 
-bool injected_alloc_failure() {
-    const char* f = std::getenv("HESS_FAULT");
-    return f && std::strcmp(f, "alloc") == 0;
-}
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -479,8 +485,19 @@ HESS_EXPORT hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens
     h->pending_dtype = dtype;
     h->pending_tokens += n_tokens;
     h->N += n_tokens;
-    if (static_cast<int>(h->pending.size()) >= h->max_pending || h->pending_tokens >= h->flush_tokens)
-        return flush_locked(h, s);
+    if (static_cast<int>(h->pending.size()) >= h->max_pending || h->pending_tokens >= h->flush_tokens) {
+        st = flush_locked(h, s);
+        if (st != HESS_OK && !h->pending.empty()) {
+            // The flush failed before launching: this call leaves no trace
+            // (the batch is neither queued nor counted); earlier batches stay
+            // queued for the next flush.
+            h->pending.pop_back();
+            h->pending_tokens -= n_tokens;
+            h->N -= n_tokens;
+            if (h->pending.empty()) h->pending_dtype = -1;
+        }
+        return st;
+    }
     return HESS_OK;
 }
 

@@ -140,13 +140,18 @@ hess_status hess_create(int64_t d, hess_t* out);
  * still queued after a call returns.
  * Errors: INVALID (NULL handle, n_tokens < 0, NULL X with n_tokens > 0,
  * unknown dtype, X not 16-byte aligned, X not device memory of the
- * handle's device or managed memory), CUDA. */
+ * handle's device or managed memory), CUDA, UNSUPPORTED (a tensor map of the
+ * flush this call triggered could not be built).  A call that fails leaves
+ * no trace: its batch is neither queued nor counted, and batches queued
+ * before it stay queued for the next flush. */
 hess_status hess_add_batch(hess_t h, const void* X, int64_t n_tokens, int32_t dtype,
                            hess_stream_t stream);
 
-/* Sum every queued batch into the accumulator now (one fused split-K pass per
- * dtype run), enqueued on `stream`, which first waits for the streams the
- * batches were added on.  No-op when nothing is queued. */
+/* Sum every queued batch into the accumulator now (one fused pass per dtype
+ * run), enqueued on `stream`, which first waits for the streams the batches
+ * were added on.  No-op when nothing is queued.  If the pass cannot be built
+ * (UNSUPPORTED: a tensor map the driver refuses), nothing is enqueued and the
+ * batches stay queued. */
 hess_status hess_flush(hess_t h, hess_stream_t stream);
 
 /* Flush, then write the damped Hessian [P4]:

@@ -201,3 +201,39 @@ def test_first_call_on_a_new_host_thread_flushes():
     o.add_batch(host(X))
     assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
     hess_destroy(h)
+
+
+def test_injected_descriptor_failure_leaves_no_trace(monkeypatch):
+    """HESS_FAULT=encode makes the tensor-map encoding of a flush fail (as
+    if the driver refused the descriptor).  The add_batch whose flush fails
+    returns HESS_ERR_UNSUPPORTED and leaves no trace (its batch neither
+    queued nor counted); the batches queued before it stay queued, and an
+    explicit flush fails the same way.  Once the fault is gone, the same
+    calls sum everything exactly once."""
+    from gptq_qqq_calibration_gb300 import Hessian, HessError
+    from gptq_qqq_calibration_gb300._lib import HESS_ERR_UNSUPPORTED
+    d = 256
+    X1, X2 = batches(d, [300, 800], seed=37)
+    h = Hessian(d, flush_tokens=1000)
+    h.add_batch(X1)
+    assert h.n_tokens == 300
+    monkeypatch.setenv("HESS_FAULT", "encode")
+    with pytest.raises(HessError) as ei:
+        h.add_batch(X2)  # 1,100 pending tokens: this call flushes
+    assert ei.value.status == HESS_ERR_UNSUPPORTED
+    assert h.n_tokens == 300
+    from gptq_qqq_calibration_gb300.hessian import hess_pending_batches
+    assert hess_pending_batches(h.handle) == 1
+    with pytest.raises(HessError) as ei:
+        h.flush()
+    assert ei.value.status == HESS_ERR_UNSUPPORTED
+    monkeypatch.delenv("HESS_FAULT")
+    h.add_batch(X2)
+    assert h.n_tokens == 1100
+    H, _ = h.materialize(0.0)
+    h.sync()
+    o = GramOracle(d)
+    o.add_batch(host(X1))
+    o.add_batch(host(X2))
+    assert rel_err(H.cpu().numpy(), o.hessian()) <= TOL_BF16
+    h.close()
