@@ -332,9 +332,12 @@ def _e2e(h, wl, xs, d, args, chunk_bytes=64 << 20):
     counts = [int(X.shape[0]) for X in xs]
     starts = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     total = int(starts[-1])
-    host_buf = torch.empty((total, d), dtype=xs[0].dtype).pin_memory()
+    # pinned at allocation, filled straight from the device copies: no
+    # pageable staging buffers are made and freed before the timed steps
+    host_buf = torch.empty((total, d), dtype=xs[0].dtype, pin_memory=True)
     for X, a in zip(xs, starts[:-1]):
-        host_buf[int(a):int(a) + X.shape[0]].copy_(X.cpu())
+        host_buf[int(a):int(a) + X.shape[0]].copy_(X)
+    torch.cuda.synchronize()
     dev_buf = torch.empty((total, d), dtype=xs[0].dtype, device="cuda")
     views = [dev_buf[int(a):int(a) + n] for a, n in zip(starts[:-1], counts)]
     # chunks: consecutive batches up to ~chunk_bytes each
@@ -351,7 +354,7 @@ def _e2e(h, wl, xs, d, args, chunk_bytes=64 << 20):
     copy_s = torch.cuda.Stream()
     comp = torch.cuda.current_stream()
     out = torch.empty((d, d), dtype=torch.float32, device="cuda")
-    host_h = torch.empty((d, d), dtype=torch.float32).pin_memory()
+    host_h = torch.empty((d, d), dtype=torch.float32, pin_memory=True)
     flops = algo_flops(wl.n_tokens, d)
 
     def step():
