@@ -80,17 +80,20 @@ def algo_flops(n_tokens, d):
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clocks, power and throttle reasons around a
+    region; summary() keeps the samples taken inside the region that
+    region_start()/region_end() bracket (host wall clock)."""
 
     def __init__(self, path):
         self.path = path
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                ["nvidia-smi", "--query-gpu=timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "20", "-i", str(self._index())],
@@ -98,6 +101,12 @@ class Clocks:
         except Exception:
             self.proc = None
         return self
+
+    def region_start(self):
+        self.t0 = time.time()
+
+    def region_end(self):
+        self.t1 = time.time()
 
     @staticmethod
     def _index():
@@ -114,14 +123,24 @@ class Clocks:
             self.f.close()
 
     def summary(self):
+        import datetime
         try:
-            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
-            sm = [float(r[1]) for r in rows]
-            mx = [float(r[2]) for r in rows]
+            rows = [[x.strip() for x in r.split(",")]
+                    for r in open(self.path).read().strip().splitlines() if r.strip()]
+            stamp = [datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp() for r in rows]
+            inside = [r for r, t in zip(rows, stamp)
+                      if self.t0 is not None and self.t1 is not None and self.t0 <= t <= self.t1]
+            window = "timed region"
+            if not inside:  # a region shorter than the sampling interval
+                inside, window = rows, "whole sampler run (no sample inside the timed region)"
+            sm = [float(r[2]) for r in inside]
+            mx = [float(r[3]) for r in rows]
+            pw = [float(r[4]) for r in inside if r[4] not in ("", "[N/A]")]
             names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-            reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].strip() == "Active"})
-            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
-                    "samples": len(rows)}
+            reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i] == "Active"})
+            return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(mx),
+                    "power_w": round(statistics.median(pw), 1) if pw else None, "reasons": reasons,
+                    "samples": len(inside), "window": window}
         except Exception as e:  # pragma: no cover
             return {"error": str(e)}
 
@@ -222,11 +241,13 @@ def run_ours(args):
     k0 = hess_kernel_launches(h.handle)  # the library's own count of its kernel launches
     with Clocks(os.path.join(tempfile.gettempdir(), f"hess_bench_clocks_rank{rank}.csv")) as clk:
         time.sleep(0.3)  # let the sampler start before the timed region
+        clk.region_start()
         e0.record()
         for k in range(args.steps):
             step(marks[k])
         e1.record()
         torch.cuda.synchronize()
+        clk.region_end()
     barrier(ws)
     kernels_timed = hess_kernel_launches(h.handle) - k0
     h.sync()  # raises if a device-side wait ran out in the timed steps
