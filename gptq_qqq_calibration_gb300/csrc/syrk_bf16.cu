@@ -175,6 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
             uint32_t phase = 0;
             int ab = 0;
             uint32_t aphase = 0;
+            // Descriptor of stage 0's first step.  Shared-memory addresses stay
+            // below 2^18, so the 14-bit address field (address / 16) takes the
+            // stage and step offsets without a carry into the next field; the
+            // additions take fewer instructions on the issuer's path than
+            // building each descriptor (measured: 1 % on the ragged stream).
+            const uint64_t desc0 = smem_desc_sw128(base, kBoxBytes, 1024u);
             for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
                 Unit un;
                 if (!syrk::unit_checked(p, u, un)) continue;
@@ -193,12 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sA = base + stage * kStageBytes;
-                        const uint32_t sB = diag ? sA : sA + kOperandBytes;
+                        // this stage's A and B descriptors: offsets added to
+                        // the address field of stage 0's (2,048 bytes per step)
+                        const uint64_t ad_s = desc0 + ((static_cast<uint32_t>(stage) * kStageBytes) >> 4);
+                        const uint64_t bd_s = diag ? ad_s : ad_s + (kOperandBytes >> 4);
 #pragma unroll
                         for (int j = 0; j < kKSteps; ++j) {
-                            const uint64_t ad = smem_desc_sw128(sA + j * 2048u, kBoxBytes, 1024u);
-                            const uint64_t bd = smem_desc_sw128(sB + j * 2048u, kBoxBytes, 1024u);
+                            const uint64_t ad = ad_s + j * (2048u >> 4);
+                            const uint64_t bd = bd_s + j * (2048u >> 4);
                             // even steps -> bank 0, odd steps -> bank 1; each bank
                             // starts afresh at the first step of the chunk.  Rows
                             // past a batch's end hold TMA's zeros and add nothing:
