@@ -59,6 +59,8 @@ def test_invalid_arguments_rejected_before_cuda(lib):
     assert lib.hess_create(-8, ctypes.byref(h)) == HESS_ERR_INVALID
     assert lib.hess_create(12, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED
     assert b"multiple of 8" in lib.hess_last_error()
+    assert lib.hess_create(32776, ctypes.byref(h)) == HESS_ERR_UNSUPPORTED  # widest is 32,768
+    assert b"exceeds 32768" in lib.hess_last_error()
     assert lib.hess_create(8, None) == HESS_ERR_INVALID
     assert lib.hess_add_batch(None, None, 4, 0, None) == HESS_ERR_INVALID
     assert lib.hess_flush(None, None) == HESS_ERR_INVALID

@@ -436,12 +436,16 @@ def test_local_zero_and_reset():
 @pytest.mark.parametrize("d,counts,dtype", [
     (16376, [300, 77, 1], torch.bfloat16),
     (12296, [40, 129], torch.float32),
+    (32768, [200, 56], torch.bfloat16),
+    (32760, [129], torch.float32),
 ])
 def test_wide_ragged_width(d, counts, dtype):
     """The widest layers: 8,256 upper tiles at d = 16,376, with a last tile
-    row 120 wide (d is a multiple of 8 but not of 128).  The oracle computes
-    a seeded sample of whole columns, the last column included, and the full
-    diagonal (which fixes the damping)."""
+    row 120 wide (d is a multiple of 8 but not of 128), and the largest width
+    a handle takes, d = 32,768 (32,896 upper tiles, a 4.3 GB accumulator),
+    with its ragged neighbour 32,760.  The oracle computes a seeded sample of
+    whole columns, the last column included, and the full diagonal (which
+    fixes the damping)."""
     from gptq_qqq_calibration_gb300 import Hessian
     cols = np.sort(np.concatenate([np.random.default_rng(7).choice(d - 1, 11, replace=False), [d - 1]]))
     h = Hessian(d)
