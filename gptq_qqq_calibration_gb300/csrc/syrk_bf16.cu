@@ -107,21 +107,25 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
     // flush of the stream may then start on the SMs this grid leaves.
     if (threadIdx.x == 0) {
         syrk::prefetch_first_map(p);
-        // The first stage's X boxes start toward L2 too.  Only L2 is
-        // touched, and it stays coherent with any write of the previous
-        // kernel still in flight: the loads after the grid wait read the
-        // finished data.
+        // The X boxes of the first unit's first ring fill (kStages stages)
+        // start toward L2 too.  Only L2 is touched, and it stays coherent
+        // with any write of the previous kernel still in flight: the loads
+        // after the grid wait read the finished data.  (Prefetching the next
+        // units' first stages as well made flushes slower: the prefetches
+        // queue ahead of the loads.)
         Unit un;
         if (static_cast<int>(blockIdx.x) < p.n_units && syrk::unit_at(p, blockIdx.x, un) &&
             syrk::unit_in_range(p, un)) {
             int b = 0;
-            while (b + 1 < p.n_batches && p.kb_start[b + 1] <= un.k0) ++b;
-            const int tok = (un.k0 - p.kb_start[b]) * kKBlock;
-            tma_prefetch_2d(&p.maps[b], un.I * kTile, tok);
-            tma_prefetch_2d(&p.maps[b], un.I * kTile + 64, tok);
-            if (un.I != un.J) {
-                tma_prefetch_2d(&p.maps[b], un.J * kTile, tok);
-                tma_prefetch_2d(&p.maps[b], un.J * kTile + 64, tok);
+            for (int kb = un.k0; kb < un.k1 && kb < un.k0 + kStages; ++kb) {
+                while (b + 1 < p.n_batches && p.kb_start[b + 1] <= kb) ++b;
+                const int tok = (kb - p.kb_start[b]) * kKBlock;
+                tma_prefetch_2d(&p.maps[b], un.I * kTile, tok);
+                tma_prefetch_2d(&p.maps[b], un.I * kTile + 64, tok);
+                if (un.I != un.J) {
+                    tma_prefetch_2d(&p.maps[b], un.J * kTile, tok);
+                    tma_prefetch_2d(&p.maps[b], un.J * kTile + 64, tok);
+                }
             }
         }
     }
