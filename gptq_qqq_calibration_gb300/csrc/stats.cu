@@ -5,6 +5,7 @@
 //     PR #3002 ("What does this PR do?") keeps as a float32 statistic because
 //     it is not a GEMM.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 
@@ -189,16 +190,29 @@ cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t
 cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
                             cudaStream_t s) {
     const int gx = (d + kColFeatures - 1) / kColFeatures;
-    // token slabs: multiples of one chain per warp, enough of them for about
-    // 8 CTAs per SM
-    const int64_t unit = static_cast<int64_t>(kColWarps) * kChain;
-    int64_t slabs = (8LL * sm_count + gx - 1) / gx;
+    // One wave: as many token slabs as the SMs hold CTAs of this kernel
+    // (4 per SM at its 64 registers per thread), split evenly, each slab a
+    // multiple of the 8 warps' token stride.  A grid of ~1.7 waves ran its
+    // second wave two-thirds full (measured: 0.72 of the HBM copy rate).
+    static std::atomic<int> resident[2] = {{0}, {0}};
+    int per_sm = resident[f32 ? 1 : 0].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        int b = 0;
+        const cudaError_t e =
+            f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<float>, kColWarps * 32, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<__nv_bfloat16>,
+                                                                kColWarps * 32, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = std::max(1, b);
+        resident[f32 ? 1 : 0].store(per_sm, std::memory_order_relaxed);
+    }
+    int64_t slabs = std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sm_count / gx);
     int64_t slab = (n + slabs - 1) / slabs;
-    slab = std::max<int64_t>(unit, ((slab + unit - 1) / unit) * unit);
+    slab = std::max<int64_t>(kColWarps, ((slab + kColWarps - 1) / kColWarps) * kColWarps);
     slabs = (n + slab - 1) / slab;
     if (slabs > 65535) {
         slabs = 65535;
-        slab = (((n + slabs - 1) / slabs + unit - 1) / unit) * unit;
+        slab = (((n + slabs - 1) / slabs + kColWarps - 1) / kColWarps) * kColWarps;
         slabs = (n + slab - 1) / slab;
     }
     const dim3 grid(gx, static_cast<unsigned>(slabs));
