@@ -78,57 +78,58 @@ __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// CTA = 256 consecutive features x one token slab; warp w takes the slab's
-// tokens w, w + 8, w + 16, ..., and lane l features 8l..8l+7 of the group, so
-// each warp reads 512 contiguous bytes of a token row (bf16).  Squares are
-// summed in fp32 chains of kChain tokens (round to nearest: unbiased), each
-// chain folded into a compensated (hi, lo) pair; the eight warps' totals are
-// added in fp64 through shared memory and the CTA adds one fp64 value per
-// feature to acc.  One atomic per feature per CTA keeps the L2 fp64 adds
-// (about 1.1 TB/s) far below the bytes streamed.
+// CTA = up to 4,096 consecutive features (thread l takes features 8l..8l+7)
+// x one token slab, so the CTA reads whole contiguous stretches of each token
+// row: a read stream over rows measured ~8 % faster on GB300 than CTAs that
+// each take a 512-byte segment of every row.  Each thread walks the slab's
+// tokens kRowsInFlight rows at a time and sums squares in fp32 chains of
+// kChain tokens (round to nearest: unbiased), each chain folded into a
+// compensated (hi, lo) pair; at the end it adds one fp64 value per feature to
+// acc, so no shared memory or barrier is needed.
 constexpr int kChain = 64;
-constexpr int kColWarps = 8;
-constexpr int kColFeatures = 256;  // features per CTA (32 lanes x 8)
+constexpr int kRowThreads = 512;                 // threads per CTA
+constexpr int kRowFeatures = kRowThreads * 8;    // features per CTA
+constexpr int kRowsInFlight = 8;
 
 template <class T>
-__global__ void __launch_bounds__(kColWarps * 32) colsumsq_kernel(const T* __restrict__ X, int64_t n, int d,
-                                                                  int64_t slab, double* __restrict__ acc) {
-    __shared__ double part[kColWarps][kColFeatures];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int f0 = blockIdx.x * kColFeatures + lane * 8;
-    const bool active = f0 < d;
+__global__ void __launch_bounds__(kRowThreads) colsumsq_kernel(const T* __restrict__ X, int64_t n, int d,
+                                                               int64_t slab, double* __restrict__ acc) {
+    const int f0 = blockIdx.x * kRowFeatures + threadIdx.x * 8;
+    if (f0 >= d) return;  // d is a multiple of 8: a thread has all 8 features or none
     const int64_t t0 = static_cast<int64_t>(blockIdx.y) * slab;
     const int64_t t1 = min(n, t0 + slab);
+    const T* const col = X + f0;
     float hi[8] = {}, lo[8] = {};
-    if (active) {
-        for (int64_t c0 = t0 + warp; c0 < t1; c0 += static_cast<int64_t>(kColWarps) * kChain) {
-            const int64_t c1 = min(t1, c0 + static_cast<int64_t>(kColWarps) * kChain);
-            float s[8] = {};
-#pragma unroll 8
-            for (int64_t t = c0; t < c1; t += kColWarps) {
-                float x[8];
-                load8(X + t * d + f0, x);
+    for (int64_t c0 = t0; c0 < t1; c0 += kChain) {
+        const int64_t c1 = min(t1, c0 + kChain);
+        float s[8] = {};
+        int64_t t = c0;
+        for (; t + kRowsInFlight <= c1; t += kRowsInFlight) {
+            float x[kRowsInFlight][8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[k], x[k], s[k]);
-            }
+            for (int r = 0; r < kRowsInFlight; ++r) load8(col + (t + r) * d, x[r]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float e;
-                hi[k] = two_sum(hi[k], s[k], e);
-                lo[k] = __fadd_rn(lo[k], e);
-            }
+            for (int r = 0; r < kRowsInFlight; ++r)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[r][k], x[r][k], s[k]);
+        }
+        for (; t < c1; ++t) {
+            float x[8];
+            load8(col + t * d, x);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s[k] = __fmaf_rn(x[k], x[k], s[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float e;
+            hi[k] = two_sum(hi[k], s[k], e);
+            lo[k] = __fadd_rn(lo[k], e);
         }
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        part[warp][lane * 8 + k] = static_cast<double>(hi[k]) + static_cast<double>(lo[k]);
-    __syncthreads();
-    const int f = blockIdx.x * kColFeatures + threadIdx.x;
-    if (f < d) {
-        double t = 0.0;
-#pragma unroll
-        for (int w = 0; w < kColWarps; ++w) t += part[w][threadIdx.x];
-        if (t != 0.0) atomicAdd(acc + f, t);
+    for (int k = 0; k < 8; ++k) {
+        const double v = static_cast<double>(hi[k]) + static_cast<double>(lo[k]);
+        if (v != 0.0) atomicAdd(acc + f0 + k, v);
     }
 }
 
@@ -189,41 +190,41 @@ cudaError_t launch_store_words(uint32_t* dst, uint32_t w0, uint32_t w1, uint32_t
 
 cudaError_t launch_colsumsq(const void* X, bool f32, int64_t n, int d, double* acc, int sm_count,
                             cudaStream_t s) {
-    const int gx = (d + kColFeatures - 1) / kColFeatures;
-    // One wave: as many token slabs as the SMs hold CTAs of this kernel
-    // (4 per SM at its 64 registers per thread), split evenly, each slab a
-    // multiple of the 8 warps' token stride.  A grid of ~1.7 waves ran its
-    // second wave two-thirds full (measured: 0.72 of the HBM copy rate).
+    const int gx = (d + kRowFeatures - 1) / kRowFeatures;
+    const int threads = std::min(kRowThreads, ((d / 8 + 31) / 32) * 32);
+    // One wave: as many token slabs as the SMs hold CTAs of this kernel,
+    // split evenly (a grid of ~1.7 waves ran its second wave two-thirds full).
     static std::atomic<int> resident[2] = {{0}, {0}};
     int per_sm = resident[f32 ? 1 : 0].load(std::memory_order_relaxed);
     if (per_sm == 0) {
         int b = 0;
         const cudaError_t e =
-            f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<float>, kColWarps * 32, 0)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<__nv_bfloat16>,
-                                                                kColWarps * 32, 0);
+            f32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<float>, kRowThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, colsumsq_kernel<__nv_bfloat16>, kRowThreads, 0);
         if (e != cudaSuccess) return e;
         per_sm = std::max(1, b);
         resident[f32 ? 1 : 0].store(per_sm, std::memory_order_relaxed);
     }
-    int64_t slabs = std::max<int64_t>(1, static_cast<int64_t>(per_sm) * sm_count / gx);
-    int64_t slab = (n + slabs - 1) / slabs;
-    slab = std::max<int64_t>(kColWarps, ((slab + kColWarps - 1) / kColWarps) * kColWarps);
+    // About 16 warps per SM: one CTA of 512 threads at d >= 4,096 (more CTAs
+    // per SM made the per-feature fp64 atomics cost more than they hid:
+    // 53.2 against 47.1 us at two per SM, measured), more for narrow rows.
+    const int ctas_per_sm = std::min(per_sm, std::max(1, kRowThreads / threads));
+    int64_t slabs = std::max<int64_t>(1, static_cast<int64_t>(ctas_per_sm) * sm_count / gx);
+    int64_t slab = std::max<int64_t>(1, (n + slabs - 1) / slabs);
     slabs = (n + slab - 1) / slab;
     if (slabs > 65535) {
         slabs = 65535;
-        slab = (((n + slabs - 1) / slabs + kColWarps - 1) / kColWarps) * kColWarps;
+        slab = (n + slabs - 1) / slabs;
         slabs = (n + slab - 1) / slab;
     }
     const dim3 grid(gx, static_cast<unsigned>(slabs));
     if (f32)
-        colsumsq_kernel<float><<<grid, kColWarps * 32, 0, s>>>(static_cast<const float*>(X), n, d, slab, acc);
+        colsumsq_kernel<float><<<grid, threads, 0, s>>>(static_cast<const float*>(X), n, d, slab, acc);
     else
         colsumsq_kernel<__nv_bfloat16>
-            <<<grid, kColWarps * 32, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n, d, slab, acc);
+            <<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(X), n, d, slab, acc);
     return cudaGetLastError();
 }
-
 cudaError_t launch_colsumsq_read(const double* acc, float* out, int d, cudaStream_t s) {
     colsumsq_read_kernel<<<(d + 255) / 256, 256, 0, s>>>(acc, out, d);
     return cudaGetLastError();
