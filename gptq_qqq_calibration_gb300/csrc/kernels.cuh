@@ -83,6 +83,8 @@ struct SyrkParams {
     float* acc;             // (hi, lo) accumulator (tile layout above)
     uint32_t* status;
     unsigned long long timeout_ns;
+    const void* l2_ptr;     // bf16 flushes of one small batch: its X (l2_bytes, a multiple of 16),
+    uint64_t l2_bytes;      // which the CTAs prefetch into L2 before the grid wait; else 0
 };
 
 // Upper-triangle tile index of tile (I, J), I <= J < T (row-major over I).

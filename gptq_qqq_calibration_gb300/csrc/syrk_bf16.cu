@@ -107,6 +107,15 @@ __global__ void __launch_bounds__(kThreads, 1) syrk_bf16_kernel(const __grid_con
     // flush of the stream may then start on the SMs this grid leaves.
     if (threadIdx.x == 0) {
         syrk::prefetch_first_map(p);
+        // A small one-batch flush: each CTA sends its share of X toward L2.
+        if (p.l2_bytes > 0) {
+            const uint64_t share = ((p.l2_bytes + gridDim.x - 1) / gridDim.x + 15) & ~15ull;
+            const uint64_t off = share * blockIdx.x;
+            if (off < p.l2_bytes) {
+                const uint64_t len = min(share, p.l2_bytes - off);
+                prefetch_l2_bulk(static_cast<const uint8_t*>(p.l2_ptr) + off, static_cast<uint32_t>(len));
+            }
+        }
         // The X boxes of the first unit's first ring fill (kStages stages)
         // start toward L2 too.  Only L2 is touched, and it stays coherent
         // with any write of the previous kernel still in flight: the loads
